@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark of the masked causal depthwise conv1d backward on GB300.
+
+One step = one mcc1d_bwd call (main kernel + gradWeight reduce) over the
+512K-token workload: S=16384, B=32 (B*S = 524288), H=4096, W=3, fp16 in and
+out, fp32 arithmetic, Bernoulli(0.9) mask, seed 0. Inputs are 12.9 GB per
+step, about 100x the 129 MB L2, so no L2 flush is needed between steps.
+
+Metric: achieved HBM bandwidth over the algorithmic bytes of a call
+(read gradY and x, write gradX, 2 bytes each per element; 1 mask byte per
+token; read weight and write gradWeight), plus tokens*H per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (the plain fp64 C restatement of the
+operation) on the host cores, one bounded sample of the workload per step.
+With N > 1 (launched by torch.distributed.run) every rank runs its own
+replica of the workload (weak scaling, no collective on the data path); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused conv1d-bwd achieved HBM GB/s and % of GB300 peak; tokens*H/sec"
+WORKLOAD = "s16384_b32_h4096_fp16"
+FALLBACK_HBM_GBS = 6800.0
+CPU_SAMPLE_S = 4096       # cpu_baseline: first 4096 positions of every batch (all H)
+REF_SAMPLE_S = 64         # --impl reference: first 64 positions per step
+E2E_STEPS = 10
+PROFILE = os.path.join(ROOT, "profiles", "mcc1d_bwd_main_s16384_b32_h4096_fp16_traffic.txt")
+KERNEL_SRC = os.path.join(ROOT, "causal_conv_backward_gb300", "csrc", "kernels.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-mask", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def aggregate(dist, seconds: float, units: float, device=None):
+    """Whole-job throughput inputs: the slowest rank's time and the units all
+    ranks processed."""
+    if dist is None:
+        return seconds, units
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.out.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.out.read())) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if "Active" in r[5 + k]
+                          and "Not" not in r[5 + k]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ helpers
+def workload(name: str, no_mask: bool):
+    import datagen
+    wl = datagen.WORKLOADS[name]
+    return wl.without_mask() if no_mask else wl
+
+
+def describe(wl) -> dict:
+    mask = "none" if wl.mask[0] == "none" else "(" + ",".join(str(v) for v in wl.mask) + ")"
+    return {"workload": wl.name, "S": wl.S, "B": wl.B, "H": wl.H, "W": wl.W, "io_dtype": wl.dtype,
+            "x_gradY": list(wl.x), "weight": list(wl.w), "mask": mask, "seed": 0,
+            "l2": f"inputs {wl.algorithmic_bytes() / 1e9:.1f} GB per step > 129 MB L2; no flush"}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the main kernel from the committed ncu summary,
+    if it was taken on the kernel source as it is now; else None."""
+    try:
+        kv = {}
+        with open(PROFILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        with open(KERNEL_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if kv.get("kernels_cu_sha256") != sha:
+            return None
+        return int(kv["dram_bytes_per_launch_full"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(wl, s_rows: int, steps: int, warmup: int):
+    """Oracle backward on the first s_rows positions of every batch; returns
+    (seconds per step, sample workload, threads used)."""
+    import datagen
+    import oracle
+    sample = wl.resized(S=s_rows)
+    inp = datagen.generate(sample, seed=0)
+    nt = oracle.threads(0)
+
+    def run():
+        oracle.bwd(sample.S, sample.B, sample.H, sample.W, sample.dtype, inp["gy"], inp["x"],
+                   inp["w"], inp["mask"], nthreads=nt)
+
+    for _ in range(warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run()
+    return (time.perf_counter() - t0) / steps, sample, nt
+
+
+# ------------------------------------------------------------------ arms
+def gpu_arm(args):
+    import numpy as np
+    import torch
+
+    import causal_conv_backward_gb300 as m
+    import datagen
+    from causal_conv_backward_gb300 import build as cbuild
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    cbuild.build()
+    m.load()
+
+    wl = workload(args.workload, args.no_mask)
+    code = m.dtype_code(wl.dtype)
+
+    def pinned(shape, dt):
+        tdt = {np.uint16: torch.int16, np.uint8: torch.uint8}[dt]
+        return torch.empty(shape, dtype=tdt, pin_memory=True)
+
+    host = datagen.generate(wl, seed=0, alloc=pinned)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+    gy = host["gy"].to(dev).view(tdt)
+    x = host["x"].to(dev).view(tdt)
+    w = host["w"].to(dev).view(tdt)
+    mask = None if host["mask"] is None else host["mask"].to(dev)
+    gx = torch.empty_like(gy)
+    gw = torch.empty_like(w)
+    nbytes = m.mcc1d_bwd_workspace_size(wl.S, wl.B, wl.H, wl.W, code, mask is not None)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        m.mcc1d_bwd(gy, x, w, mask, gx, gw, ws, stream, wl.S, wl.B, wl.H, wl.W, code, nbytes)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if m.mcc1d_bwd_device_status(ws, stream) != 0:
+        raise SystemExit("bench.py: device-side status is not OK")
+
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    sampler = ClockSampler(f"GPU-{gpu_id}" if gpu_id is not None else str(local))
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.05)
+    start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(dist, dev)
+    elapsed = start.elapsed_time(end) / 1e3
+    per_call = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    alg = wl.algorithmic_bytes()
+    t_max, bytes_all = aggregate(dist, elapsed, float(alg) * K, dev)
+    value = bytes_all / t_max / 1e9
+    tokens_h = float(wl.E) * K * world / t_max
+
+    # end to end: pinned host inputs -> device -> call -> host outputs, every step
+    e2e = None
+    if not args.no_e2e:
+        hx = {k: v for k, v in host.items() if v is not None}
+        out_gx = torch.empty(gx.shape, dtype=torch.int16, pin_memory=True)
+        out_gw = torch.empty(gw.shape, dtype=torch.int16, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in hx.values())
+        d2h = out_gx.numel() * 2 + out_gw.numel() * 2
+
+        def e2e_step():
+            gy.view(torch.int16).copy_(hx["gy"], non_blocking=True)
+            x.view(torch.int16).copy_(hx["x"], non_blocking=True)
+            w.view(torch.int16).copy_(hx["w"], non_blocking=True)
+            if mask is not None:
+                mask.copy_(hx["mask"], non_blocking=True)
+            step()
+            out_gx.copy_(gx.view(torch.int16), non_blocking=True)
+            out_gw.copy_(gw.view(torch.int16), non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        n = min(E2E_STEPS, K)
+        barrier(dist, dev)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        te, be = aggregate(dist, a.elapsed_time(b) / 1e3, float(alg) * n, dev)
+        e2e = {"value": round(be / te / 1e9, 2), "unit": "GB/s", "steps": n,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(te / n * 1e3, 3)}
+
+    peak, peak_kind = measured_peak()
+    avg_call = sum(per_call) / len(per_call)
+    achieved = alg / avg_call / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "kernel": "mcc1d_bwd_main (timed as the whole call: main + reduce)",
+                "algorithmic_bytes_per_launch": alg,
+                "median_call_ms": round(statistics.median(per_call) * 1e3, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t, sample, nt = time_oracle(wl, CPU_SAMPLE_S, steps=1, warmup=0)
+        cpu = {"value": round(sample.algorithmic_bytes() / t / 1e9, 4), "unit": "GB/s",
+               "cores": nt, "kind": "oracle",
+               "sample": f"first {sample.S} of {wl.S} positions of all {wl.B} batches, all H "
+                         f"({sample.E} elements), one pass, {t:.2f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(t_max / K * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generator; fp16 bit patterns)",
+            "config": describe(wl), "tokens_h_per_s": float(f"{tokens_h:.4e}"),
+            "frac_of_peak": round(value / world / peak, 4),
+            "e2e": e2e, "gpu_launches": 2 * K, "roofline": roofline, "cpu_baseline": cpu,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl = workload(args.workload, args.no_mask)
+    K = args.steps
+    t, sample, nt = time_oracle(wl, REF_SAMPLE_S, steps=K, warmup=max(0, args.warmup))
+    value = sample.algorithmic_bytes() / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator; fp16 bit patterns)", "config": describe(wl),
+        "tokens_h_per_s": float(f"{sample.E / t:.4e}"),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nt, "kind": "oracle",
+                         "sample": f"per step: first {sample.S} of {wl.S} positions of all "
+                                   f"{wl.B} batches, all H ({sample.E} elements)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,18 @@
+"""Masked causal depthwise conv1d backward (W = 3) for NVIDIA GB300.
+
+Thin ctypes binding over ``libmcc1d.so`` (see ``include/mcc1d.h``). The names
+mirror the C ABI; the binding only marshals arguments. Every step of the
+computation runs in the library's CUDA kernels: there is no CPU or PyTorch
+fallback, and a missing library is an error.
+
+Torch tensors may be passed for device buffers; their ``data_ptr()`` is
+handed to the C ABI, and torch is used for nothing else. ``backward`` is a
+convenience wrapper that allocates outputs and workspace with torch.
+"""
+from __future__ import annotations
+
+from ._lib import (  # noqa: F401
+    BF16, FP16, Mcc1dError, STATUS, backward, dtype_code, lib_path, load,
+    mcc1d_bwd, mcc1d_bwd_device_status, mcc1d_bwd_workspace_size, mcc1d_status_string,
+    mcc1d_version,
+)

@@ -1,0 +1,145 @@
+"""ctypes binding of libmcc1d.so: argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+BF16, FP16 = 0, 1
+STATUS = {
+    0: "MCC1D_OK",
+    161001: "MCC1D_ERR_PARAM_NULLPTR",
+    161002: "MCC1D_ERR_PARAM_INVALID",
+    561002: "MCC1D_ERR_INNER_TILING_ERROR",
+    561003: "MCC1D_ERR_WORKSPACE",
+    561100: "MCC1D_ERR_CUDA",
+    561101: "MCC1D_ERR_DEVICE_TIMEOUT",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Mcc1dError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, 'unknown')} ({self.status})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libmcc1d.so (it must have been built: ``__graft_entry__.build()``
+    or ``python -m causal_conv_backward_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"libmcc1d.so is not built ({_build.LIB}); "
+                               "run causal_conv_backward_gb300.build.build() first")
+        lib = ctypes.CDLL(_build.LIB)
+        i64, i32, u64, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p
+        lib.mcc1d_bwd_workspace_size.argtypes = [i64, i64, i64, i64, i32, i32, ctypes.POINTER(u64)]
+        lib.mcc1d_bwd_workspace_size.restype = i32
+        lib.mcc1d_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, u64]
+        lib.mcc1d_bwd.restype = i32
+        lib.mcc1d_bwd_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+        lib.mcc1d_bwd_device_status.restype = i32
+        lib.mcc1d_status_string.argtypes = [i32]
+        lib.mcc1d_status_string.restype = ctypes.c_char_p
+        lib.mcc1d_version.argtypes = []
+        lib.mcc1d_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return a.data_ptr()
+
+
+def dtype_code(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    name = str(dtype).replace("torch.", "")
+    return {"bf16": BF16, "bfloat16": BF16, "fp16": FP16, "float16": FP16, "half": FP16}[name]
+
+
+def mcc1d_bwd_workspace_size(S, B, H, W, dtype, has_mask) -> int:
+    out = ctypes.c_uint64(0)
+    st = load().mcc1d_bwd_workspace_size(S, B, H, W, dtype_code(dtype), int(bool(has_mask)),
+                                         ctypes.byref(out))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_bwd_workspace_size")
+    return int(out.value)
+
+
+def mcc1d_bwd(gradY, x, weight, mask_or_null, gradX, gradWeight, workspace, stream,
+              S, B, H, W, dtype, workspace_bytes) -> None:
+    """Enqueue the backward; buffers are device pointers (ints) or tensors,
+    ``stream`` a cudaStream_t as int (0 = legacy default) or a torch stream."""
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = load().mcc1d_bwd(_ptr(gradY), _ptr(x), _ptr(weight), _ptr(mask_or_null), _ptr(gradX),
+                          _ptr(gradWeight), _ptr(workspace), stream or None, S, B, H, W,
+                          dtype_code(dtype), int(workspace_bytes))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_bwd")
+
+
+def mcc1d_bwd_device_status(workspace, stream=None) -> int:
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    out = ctypes.c_int32(-1)
+    st = load().mcc1d_bwd_device_status(_ptr(workspace), stream or None, ctypes.byref(out))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_bwd_device_status")
+    return int(out.value)
+
+
+def mcc1d_status_string(status: int) -> str:
+    return load().mcc1d_status_string(int(status)).decode()
+
+
+def mcc1d_version() -> int:
+    return int(load().mcc1d_version())
+
+
+def backward(gradY, x, weight, mask=None, *, gradX=None, gradWeight=None, workspace=None,
+             stream=None):
+    """Convenience call on torch CUDA tensors: gradY, x [S,B,H], weight [3,H]
+    (bf16 or fp16), mask [B,S] bool/uint8 or None. Allocates whatever output
+    or workspace is not given (with torch) and returns (gradX, gradWeight)."""
+    import torch
+
+    S, B, H = gradY.shape
+    W = weight.shape[0]
+    code = dtype_code(gradY.dtype)
+    for t in (gradY, x, weight):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("gradY, x and weight must be contiguous CUDA tensors")
+    if mask is not None:
+        if mask.dtype == torch.bool:
+            mask = mask.view(torch.uint8)
+        if not mask.is_contiguous():
+            raise ValueError("mask must be contiguous")
+    if gradX is None:
+        gradX = torch.empty_like(gradY)
+    if gradWeight is None:
+        gradWeight = torch.empty_like(weight)
+    nbytes = mcc1d_bwd_workspace_size(S, B, H, W, code, mask is not None)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=gradY.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(gradY.device)
+    mcc1d_bwd(gradY, x, weight, mask, gradX, gradWeight, workspace, stream, S, B, H, W, code,
+              workspace.numel() * workspace.element_size())
+    return gradX, gradWeight

@@ -1,0 +1,719 @@
+// kernels.cu - sm_103a kernels of the masked causal depthwise conv1d backward.
+//
+// Operation (CANN operator page "aclnnMaskedCausalConv1dBackward", 功能说明 /
+// 计算公式), for every depthwise channel h:
+//   gYm(i,j)      = mask(j,i) * gradY(i,j)
+//   gradX(i,j)    = gYm(i,j)*w(2) + gYm(i+1,j)*w(1) + gYm(i+2,j)*w(0)
+//   gradWeight(k) = sum_{j,i} gYm(i+2-k,j) * x(i,j)
+// with gYm zero for i >= S.
+//
+// The work is pure streaming: each element of gradY and x is read once and
+// each element of gradX written once, at 12 flops per 6 bytes, so the bound is
+// HBM bandwidth and there is no dense contraction for the tensor cores.
+//
+// mcc1d_bwd_main (persistent, one range of rows per CTA):
+//   The rows (hb, j, i) - H-block, batch, sequence position, i fastest - are
+//   split into ncta contiguous ranges. Warp 0 is the producer: it walks its
+//   CTA's range in stages of R rows and, per stage, copies the R rows of x and
+//   the R rows of gradY two positions ahead (plus the first two rows when a
+//   sequence starts) into a ring slot with cp.async.bulk, completing on the
+//   slot's "full" mbarrier; it also stores the stage's mask bytes in the slot.
+//   The consumer warps own one 16-byte vector (8 channels) each, keep the last
+//   two masked gradY rows in registers, and per row form gradX with a
+//   compensated three-term sum (exact fp32 products + TwoSum), store it with
+//   a streaming 16-byte store, and accumulate the three gradWeight taps in
+//   fp32. Each CTA writes one fp32 partial [3][H-block] per H-block it
+//   touched into the workspace.
+// mcc1d_bwd_reduce (programmatic dependent launch):
+//   Sums the partials of every gradWeight column in a fixed order (32 serial
+//   splits over the CTAs, then a pairwise tree), rounds once to the 16-bit
+//   type and folds the CTAs' status words into the workspace header.
+//
+// Every device-side wait is bounded (kWaitLimitNs); a CTA whose wait gives up
+// stops, waits (bounded) for its own bulk copies to land and reports
+// kErrTimeout through its status word instead of hanging.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "launch.h"
+#include "plan.h"
+
+namespace mcc1d {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kMaxThreads = 160;                  // 4 consumer warps + producer
+
+struct MainParams {
+    const uint8_t *gy;     // [S,B,H] 16-bit elements, addressed in bytes
+    const uint8_t *x;      // [S,B,H]
+    const uint16_t *w;     // [3,H]
+    const uint8_t *mask;   // [B,S] or null
+    uint8_t *gx;           // [S,B,H]
+    float *part;           // [ncta][maxseg][3][hb_width]
+    int32_t *status;       // [ncta]
+    int64_t S, BS, H, N;
+    int32_t B, hb_width, ncta, maxseg, stages;
+    uint32_t row_bytes, slot_bytes, off_mask, off_bar, off_outer;
+};
+
+struct ReduceParams {
+    const float *part;
+    const int32_t *status;
+    int32_t *header;
+    uint8_t *gw;           // [3,H]
+    int64_t N, BS, H;
+    int32_t hb_width, ncta, maxseg, nchunk;
+    int32_t c_lo[kMaxHb], c_hi[kMaxHb];
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of `bar` with the given parity to complete; gives up
+// (returns false) after kWaitLimitNs.
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+// Global -> shared bulk copy completing on an mbarrier (no multicast).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Packed fp32x2 arithmetic (sm_100+), each lane rounded to nearest even.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// ------------------------------------------------------------------ 16-bit types
+// DT 0 = bf16, 1 = fp16. Eight channels travel as one uint4 (16 bytes).
+struct V8 {
+    float2 e[4];
+};
+
+template <int DT>
+__device__ __forceinline__ float2 unpack2(uint32_t u)
+{
+    if (DT == 0) {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    } else {
+        union {
+            uint32_t u;
+            __half2 h;
+        } c;
+        c.u = u;
+        return __half22float2(c.h);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float2 v)
+{
+    if (DT == 0) {
+        union {
+            __nv_bfloat162 b;
+            uint32_t u;
+        } c;
+        c.b = __floats2bfloat162_rn(v.x, v.y);
+        return c.u;
+    } else {
+        union {
+            __half2 h;
+            uint32_t u;
+        } c;
+        c.h = __floats2half2_rn(v.x, v.y);
+        return c.u;
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ V8 unpack8(uint4 u)
+{
+    V8 v;
+    v.e[0] = unpack2<DT>(u.x);
+    v.e[1] = unpack2<DT>(u.y);
+    v.e[2] = unpack2<DT>(u.z);
+    v.e[3] = unpack2<DT>(u.w);
+    return v;
+}
+
+// A staged gradY row, masked by clearing the bits (exact +0 whatever the
+// staged bytes hold; rows past the end of S carry a zero mask byte).
+template <int DT>
+__device__ __forceinline__ V8 load_masked(const uint8_t *p, uint8_t keep_byte)
+{
+    uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t keep = 0u - (uint32_t)keep_byte;
+    u.x &= keep;
+    u.y &= keep;
+    u.z &= keep;
+    u.w &= keep;
+    return unpack8<DT>(u);
+}
+
+// ------------------------------------------------------------------ row cursor
+// Position in the flattened (hb, j, i) row sequence of one CTA range.
+struct Cursor {
+    int64_t pos, end, i;
+    int32_t j, hb;
+
+    __device__ __forceinline__ void init(int64_t r0, int64_t r1, int64_t S, int64_t BS)
+    {
+        pos = r0;
+        end = r1;
+        hb = (int32_t)(r0 / BS);
+        const int64_t rem = r0 - (int64_t)hb * BS;
+        j = (int32_t)(rem / S);
+        i = rem - (int64_t)j * S;
+    }
+    // Rows of the next stage: at most R, never across a sequence end or the range end.
+    template <int R>
+    __device__ __forceinline__ int rows(int64_t S) const
+    {
+        int64_t n = S - i;
+        if (end - pos < n)
+            n = end - pos;
+        return n < R ? (int)n : R;
+    }
+    __device__ __forceinline__ void advance(int n, int64_t S, int32_t B)
+    {
+        pos += n;
+        i += n;
+        if (i == S) {
+            i = 0;
+            if (++j == B) {
+                j = 0;
+                ++hb;
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ producer
+template <int R>
+__device__ __forceinline__ uint32_t stage_mask_byte(const MainParams &p, const Cursor &c, int lane)
+{
+    if (lane >= R + 2)
+        return 0;
+    const int64_t row = c.i + lane;
+    if (row >= p.S)
+        return 0;  // past the end of the sequence: zero padding
+    if (p.mask == nullptr)
+        return 1;
+    return __ldg(p.mask + (int64_t)c.j * p.S + row) != 0 ? 1u : 0u;
+}
+
+template <int R>
+__device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t r1, int lane)
+{
+    const int NS = p.stages;
+    const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
+    const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
+    const uint32_t ring0 = smem_u32(smem);
+    const int64_t row_elems = (int64_t)p.B * p.H;  // elements between rows i and i+1
+
+    Cursor cur;
+    cur.init(r0, r1, p.S, p.BS);
+    int slot = 0, stage = 0;
+    uint32_t ph = 0;
+    bool dead = false;
+    uint32_t mnext = stage_mask_byte<R>(p, cur, lane);
+    while (cur.pos < r1) {
+        const int n = cur.rows<R>(p.S);
+        const bool head = (stage == 0) || (cur.i == 0);
+        const uint32_t mcur = mnext;
+        if (stage >= NS) {
+            const bool ok = mbar_wait_bounded(bar_empty0 + 8u * slot, ph ^ 1u);
+            dead = __any_sync(0xFFFFFFFFu, !ok);
+            if (dead)
+                break;
+        }
+        if (lane < R + 2)
+            smem[p.off_mask + 32u * slot + lane] = (uint8_t)mcur;
+        {
+            Cursor nx = cur;
+            nx.advance(n, p.S, p.B);
+            if (nx.pos < r1)
+                mnext = stage_mask_byte<R>(p, nx, lane);
+        }
+        const int64_t hb0 = (int64_t)cur.hb * p.hb_width;
+        const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
+        const uint32_t wbytes = (uint32_t)width * 2u;
+        const int q0 = head ? 0 : 2;           // first gradY slot row this stage loads
+        int64_t q1 = (int64_t)n + 2;           // gradY slot rows [q0, q1) lie inside S
+        if (p.S - cur.i < q1)
+            q1 = p.S - cur.i;
+        const int nG = q1 > q0 ? (int)(q1 - q0) : 0;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar_full0 + 8u * slot, (uint32_t)(nG + n) * wbytes);
+        __syncwarp();
+        const uint32_t slot_base = ring0 + (uint32_t)slot * p.slot_bytes;
+        if (lane < nG) {
+            const int q = q0 + lane;
+            const int64_t e = ((cur.i + q) * p.B + cur.j) * p.H + hb0;
+            bulk_g2s(slot_base + (uint32_t)q * p.row_bytes, p.gy + 2 * e, wbytes, bar_full0 + 8u * slot);
+        } else if (lane < nG + n) {
+            const int q = lane - nG;
+            const int64_t e = (cur.i + q) * row_elems + (int64_t)cur.j * p.H + hb0;
+            bulk_g2s(slot_base + (uint32_t)(R + 2 + q) * p.row_bytes, p.x + 2 * e, wbytes,
+                     bar_full0 + 8u * slot);
+        }
+        cur.advance(n, p.S, p.B);
+        ++stage;
+        if (++slot == NS) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+    // Drain: every slot's last issued stage must have landed before the CTA
+    // may exit (no-op in a normal run, where the consumers saw them all).
+    const int used = stage < NS ? stage : NS;
+    for (int s = 0; s < used; ++s) {
+        const int last = s + NS * ((stage - 1 - s) / NS);
+        if (!mbar_wait_bounded(bar_full0 + 8u * s, (uint32_t)((last / NS) & 1)))
+            dead = true;
+    }
+    return __any_sync(0xFFFFFFFFu, dead);
+}
+
+// ------------------------------------------------------------------ consumers
+template <int DT, int R>
+__device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t r1, int ct, int lane)
+{
+    const int NS = p.stages;
+    const int nct = (int)blockDim.x - 32;
+    const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
+    const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
+    float *outer = reinterpret_cast<float *>(smem + p.off_outer);  // [24][nct]
+    const int64_t row_stride = 2 * (int64_t)p.B * p.H;             // bytes from row i to i+1
+    const int c = blockIdx.x;
+
+    Cursor cur;
+    cur.init(r0, r1, p.S, p.BS);
+    const int hb_first = cur.hb;
+    int hb_cur = -1;
+    bool active = false;
+    V8 w0, w1, w2;
+    float2 mid[3][4];
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            mid[k][e] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 24; ++q)
+        outer[q * nct + ct] = 0.f;
+    int since_flush = 0;
+    V8 g0, g1;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        g0.e[e] = g1.e[e] = make_float2(0.f, 0.f);
+
+    // Writes this thread's share of the partial for H-block hb_cur and clears
+    // the accumulators. Sum order: shared-memory level, then register level.
+    auto flush_partial = [&]() {
+        if (active) {
+            float *dst = p.part +
+                         (((int64_t)c * p.maxseg + (hb_cur - hb_first)) * 3) * p.hb_width + 8 * ct;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[2 * e] = outer[(k * 8 + 2 * e) * nct + ct] + mid[k][e].x;
+                    v[2 * e + 1] = outer[(k * 8 + 2 * e + 1) * nct + ct] + mid[k][e].y;
+                }
+                float4 *d4 = reinterpret_cast<float4 *>(dst + (int64_t)k * p.hb_width);
+                d4[0] = make_float4(v[0], v[1], v[2], v[3]);
+                d4[1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                mid[k][e] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 24; ++q)
+            outer[q * nct + ct] = 0.f;
+        since_flush = 0;
+    };
+
+    int slot = 0, stage = 0;
+    uint32_t ph = 0;
+    bool dead = false;
+    while (cur.pos < r1) {
+        const int n = cur.rows<R>(p.S);
+        const bool head = (stage == 0) || (cur.i == 0);
+        if (cur.hb != hb_cur) {
+            if (hb_cur >= 0)
+                flush_partial();
+            hb_cur = cur.hb;
+            const int64_t hb0 = (int64_t)hb_cur * p.hb_width;
+            const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
+            active = 8 * ct < width;
+            if (active) {
+                w0 = unpack8<DT>(__ldg(reinterpret_cast<const uint4 *>(p.w + 0 * p.H + hb0 + 8 * ct)));
+                w1 = unpack8<DT>(__ldg(reinterpret_cast<const uint4 *>(p.w + 1 * p.H + hb0 + 8 * ct)));
+                w2 = unpack8<DT>(__ldg(reinterpret_cast<const uint4 *>(p.w + 2 * p.H + hb0 + 8 * ct)));
+            }
+        }
+        if (!dead) {
+            const bool ok = mbar_wait_bounded(bar_full0 + 8u * slot, ph);
+            dead = __any_sync(0xFFFFFFFFu, !ok);
+        }
+        if (!dead && active) {
+            const uint8_t *sl = smem + (size_t)slot * p.slot_bytes + 16 * ct;
+            const uint8_t *gys = sl;                              // gradY slot rows 0..R+1
+            const uint8_t *xs = sl + (size_t)(R + 2) * p.row_bytes;  // x slot rows 0..R-1
+            const uint8_t *ms = smem + p.off_mask + 32u * slot;
+            if (head) {
+                g0 = load_masked<DT>(gys, ms[0]);
+                g1 = load_masked<DT>(gys + p.row_bytes, ms[1]);
+            }
+            uint8_t *gxp = p.gx + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + 8 * ct);
+            float2 in[3][4];
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    in[k][e] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (r < n) {
+                    const V8 g2 = load_masked<DT>(gys + (size_t)(r + 2) * p.row_bytes, ms[r + 2]);
+                    const V8 xv = unpack8<DT>(*reinterpret_cast<const uint4 *>(xs + (size_t)r * p.row_bytes));
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        // gradX: products of two 16-bit values are exact in fp32;
+                        // s + err == p0 + p1 exactly (TwoSum), then one more add
+                        // and the correction: within a hair of the exact sum.
+                        const float2 p0 = mul2(g0.e[e], w2.e[e]);
+                        const float2 p1 = mul2(g1.e[e], w1.e[e]);
+                        const float2 p2 = mul2(g2.e[e], w0.e[e]);
+                        const float2 s = add2(p0, p1);
+                        const float2 bb = sub2(s, p0);
+                        const float2 err = add2(sub2(p0, sub2(s, bb)), sub2(p1, bb));
+                        const float2 t = add2(s, p2);
+                        o[e] = pack2<DT>(add2(t, err));
+                        // gradWeight taps: k = 2 pairs x(i) with gYm(i), k = 1
+                        // with gYm(i+1), k = 0 with gYm(i+2).
+                        in[2][e] = fma2(g0.e[e], xv.e[e], in[2][e]);
+                        in[1][e] = fma2(g1.e[e], xv.e[e], in[1][e]);
+                        in[0][e] = fma2(g2.e[e], xv.e[e], in[0][e]);
+                    }
+                    __stcs(reinterpret_cast<uint4 *>(gxp + (int64_t)r * row_stride),
+                           make_uint4(o[0], o[1], o[2], o[3]));
+                    g0 = g1;
+                    g1 = g2;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    mid[k][e] = add2(mid[k][e], in[k][e]);
+            if (++since_flush == kFlushStages) {
+#pragma unroll
+                for (int k = 0; k < 3; ++k)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        outer[(k * 8 + 2 * e) * nct + ct] += mid[k][e].x;
+                        outer[(k * 8 + 2 * e + 1) * nct + ct] += mid[k][e].y;
+                        mid[k][e] = make_float2(0.f, 0.f);
+                    }
+                since_flush = 0;
+            }
+        }
+        __syncwarp();
+        if (!dead && lane == 0)
+            mbar_arrive(bar_empty0 + 8u * slot);
+        cur.advance(n, p.S, p.B);
+        ++stage;
+        if (++slot == NS) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+    if (hb_cur >= 0)
+        flush_partial();
+    return dead;
+}
+
+// ------------------------------------------------------------------ kernels
+template <int DT, int R>
+__global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_constant__ MainParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_err;
+    const int c = blockIdx.x;
+    const int64_t r0 = cta_row_begin(c, p.N, p.ncta);
+    const int64_t r1 = cta_row_begin(c + 1, p.N, p.ncta);
+    const int consumer_warps = (int)(blockDim.x >> 5) - 1;
+    if (threadIdx.x == 0) {
+        s_err = 0;
+        const uint32_t bar0 = smem_u32(smem + p.off_bar);
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(bar0 + 8u * s, 1);                                    // full
+            mbar_init(bar0 + 8u * (p.stages + s), (uint32_t)consumer_warps);  // empty
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    // Let the reduce kernel's CTAs be scheduled as this grid retires; it
+    // waits for this grid's completion before touching the partials.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const int lane = threadIdx.x & 31;
+    bool dead;
+    if (threadIdx.x < 32)
+        dead = produce<R>(p, smem, r0, r1, lane);
+    else
+        dead = consume<DT, R>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
+    if (dead && lane == 0)
+        atomicOr(&s_err, 1);
+    __syncthreads();
+    if (threadIdx.x == 0)
+        p.status[c] = s_err ? kErrTimeout : kOk;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kReduceWarps * 32) mcc1d_bwd_reduce(const __grid_constant__ ReduceParams p)
+{
+    __shared__ float4 red[kReduceWarps][32];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x;
+    const int chunk = b % p.nchunk;
+    const int k = (b / p.nchunk) % 3;
+    const int hb = b / (p.nchunk * 3);
+    const int64_t hb0 = (int64_t)hb * p.hb_width;
+    const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
+    const int col = chunk * kReduceCols + 4 * lane;
+    const int clo = p.c_lo[hb], nc = p.c_hi[hb] - p.c_lo[hb] + 1;
+    const int cb = clo + (int)((int64_t)warp * nc / kReduceWarps);
+    const int ce = clo + (int)((int64_t)(warp + 1) * nc / kReduceWarps);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col < width) {
+        for (int cc = cb; cc < ce; ++cc) {
+            const int seg = hb - (int)(cta_row_begin(cc, p.N, p.ncta) / p.BS);
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(
+                p.part + (((int64_t)cc * p.maxseg + seg) * 3 + k) * p.hb_width + col));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+    }
+    red[warp][lane] = acc;
+    __syncthreads();
+#pragma unroll
+    for (int s = kReduceWarps / 2; s >= 1; s >>= 1) {
+        if (warp < s) {
+            float4 a = red[warp][lane];
+            const float4 o = red[warp + s][lane];
+            a.x += o.x;
+            a.y += o.y;
+            a.z += o.z;
+            a.w += o.w;
+            red[warp][lane] = a;
+        }
+        __syncthreads();
+    }
+    if (warp == 0 && col < width) {
+        const float4 a = red[0][lane];
+        const uint32_t lo = pack2<DT>(make_float2(a.x, a.y));
+        const uint32_t hi = pack2<DT>(make_float2(a.z, a.w));
+        *reinterpret_cast<uint2 *>(p.gw + 2 * ((int64_t)k * p.H + hb0 + col)) = make_uint2(lo, hi);
+    }
+    if (b == 0) {
+        int any = 0;
+        for (int cc = threadIdx.x; cc < p.ncta; cc += blockDim.x)
+            any |= (p.status[cc] != kOk);
+        any = __syncthreads_or(any);
+        if (threadIdx.x == 0)
+            p.header[0] = any ? kErrTimeout : kOk;
+    }
+}
+
+// ------------------------------------------------------------------ host launch
+typedef void (*MainFn)(MainParams);
+typedef void (*ReduceFn)(ReduceParams);
+
+template <int DT>
+static MainFn main_for(int R)
+{
+    switch (R) {
+    case 4: return mcc1d_bwd_main<DT, 4>;
+    case 6: return mcc1d_bwd_main<DT, 6>;
+    case 8: return mcc1d_bwd_main<DT, 8>;
+    default: return nullptr;
+    }
+}
+
+// cudaFuncSetAttribute once per (kernel, device).
+static bool ensure_smem_attr(const void *fn, int slot_id)
+{
+    static std::atomic<uint64_t> done[8];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done[slot_id].load(std::memory_order_acquire) & bit)
+        return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCtaMax) !=
+        cudaSuccess)
+        return false;
+    done[slot_id].fetch_or(bit, std::memory_order_acq_rel);
+    return true;
+}
+
+int32_t launch_bwd(const Plan &pl, const void *gradY, const void *x, const void *weight,
+                   const uint8_t *mask, void *gradX, void *gradWeight, void *workspace,
+                   cudaStream_t stream)
+{
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    MainParams mp;
+    mp.gy = static_cast<const uint8_t *>(gradY);
+    mp.x = static_cast<const uint8_t *>(x);
+    mp.w = static_cast<const uint16_t *>(weight);
+    mp.mask = mask;
+    mp.gx = static_cast<uint8_t *>(gradX);
+    mp.part = reinterpret_cast<float *>(ws + pl.ws_part_off);
+    mp.status = reinterpret_cast<int32_t *>(ws + pl.ws_status_off);
+    mp.S = pl.S;
+    mp.BS = pl.B * pl.S;
+    mp.H = pl.H;
+    mp.N = pl.rows_total;
+    mp.B = (int32_t)pl.B;
+    mp.hb_width = pl.hb_width;
+    mp.ncta = pl.ncta;
+    mp.maxseg = pl.maxseg;
+    mp.stages = pl.stages;
+    mp.row_bytes = pl.row_bytes;
+    mp.slot_bytes = pl.slot_bytes;
+    mp.off_mask = pl.off_mask;
+    mp.off_bar = pl.off_bar;
+    mp.off_outer = pl.off_outer;
+
+    ReduceParams rp;
+    rp.part = mp.part;
+    rp.status = mp.status;
+    rp.header = reinterpret_cast<int32_t *>(ws);
+    rp.gw = static_cast<uint8_t *>(gradWeight);
+    rp.N = pl.rows_total;
+    rp.BS = pl.B * pl.S;
+    rp.H = pl.H;
+    rp.hb_width = pl.hb_width;
+    rp.ncta = pl.ncta;
+    rp.maxseg = pl.maxseg;
+    rp.nchunk = (pl.hb_width + kReduceCols - 1) / kReduceCols;
+    for (int h = 0; h < kMaxHb; ++h) {
+        rp.c_lo[h] = pl.c_lo[h];
+        rp.c_hi[h] = pl.c_hi[h];
+    }
+
+    const int R = pl.rows_per_stage;
+    MainFn mfn = pl.dtype == 0 ? main_for<0>(R) : main_for<1>(R);
+    ReduceFn rfn = pl.dtype == 0 ? mcc1d_bwd_reduce<0> : mcc1d_bwd_reduce<1>;
+    if (!mfn)
+        return kErrCuda;
+    const int attr_slot = pl.dtype * 3 + (R == 4 ? 0 : R == 6 ? 1 : 2);
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(mfn), attr_slot))
+        return kErrCuda;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.ncta);
+    cfg.blockDim = dim3((unsigned)pl.threads);
+    cfg.dynamicSmemBytes = pl.smem_bytes;
+    cfg.stream = stream;
+    if (cudaLaunchKernelEx(&cfg, mfn, mp) != cudaSuccess)
+        return kErrCuda;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t rcfg = {};
+    rcfg.gridDim = dim3((unsigned)pl.reduce_blocks);
+    rcfg.blockDim = dim3(kReduceWarps * 32);
+    rcfg.dynamicSmemBytes = 0;
+    rcfg.stream = stream;
+    rcfg.attrs = attr;
+    rcfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&rcfg, rfn, rp) != cudaSuccess)
+        return kErrCuda;
+    return kOk;
+}
+
+}  // namespace mcc1d

@@ -1,0 +1,118 @@
+// plan.cpp - shape validation and the launch plan (host only, no CUDA).
+#include "plan.h"
+
+#include <string.h>
+
+namespace mcc1d {
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Limits from the operator page's constraints (约束说明): B in [1,32],
+// B*S in [1, 512K], H in [384, 24576] and a multiple of 64, W == 3; and the
+// two 16-bit types of its parameter table (参数说明).
+int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype)
+{
+    if (dtype != 0 && dtype != 1)
+        return kErrInvalid;
+    if (W != kW)
+        return kErrShape;
+    if (B < 1 || B > 32 || S < 1 || S > 524288 || B * S > 524288)
+        return kErrShape;
+    if (H < 384 || H > 24576 || H % 64 != 0)
+        return kErrShape;
+    return kOk;
+}
+
+int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p)
+{
+    int32_t st = validate_shape(S, B, H, W, dtype);
+    if (st != kOk)
+        return st;
+    memset(p, 0, sizeof(*p));
+    p->S = S;
+    p->B = B;
+    p->H = H;
+    p->dtype = dtype;
+
+    // H-blocks: as few as possible of at most 1024 halves, balanced, each a
+    // multiple of 64 halves so every staged row is a multiple of 128 bytes.
+    p->n_hb = (int32_t)ceil_div(H, kMaxHbWidth);
+    p->hb_width = (int32_t)round_up(ceil_div(H, p->n_hb), 64);
+    const int vectors = p->hb_width / 8;
+    p->consumer_warps = (int32_t)ceil_div(vectors, 32);
+    p->threads = 32 * (p->consumer_warps + 1);
+
+    // Aim for at least 8 consumer warps per SM.
+    int cps = (int)ceil_div(8, p->consumer_warps);
+    while (cps > 1 && cps * p->threads > 2048)
+        --cps;
+    p->ctas_per_sm = cps;
+
+    p->row_bytes = (uint32_t)p->hb_width * 2u;
+    const uint32_t outer_bytes = (uint32_t)p->consumer_warps * 32u * 24u * 4u;
+    const int64_t budget = kSmemPerSM / cps - kSmemReservedPerCta;
+
+    // Rows per stage and ring depth: the deepest R (fewer barrier round trips)
+    // that still leaves a ring of three slots, else R = 4 with what fits.
+    const int r_choices[3] = {8, 6, 4};
+    p->rows_per_stage = 0;
+    for (int t = 0; t < 3; ++t) {
+        const int R = r_choices[t];
+        const int64_t slot = (int64_t)(2 * R + 2) * p->row_bytes;
+        int64_t ns = (budget - outer_bytes - 64) / (slot + 48);
+        if (ns >= 3 || t == 2) {
+            if (ns > 6)
+                ns = 6;
+            if (ns < 2)
+                ns = 2;
+            p->rows_per_stage = R;
+            p->stages = (int32_t)ns;
+            p->slot_bytes = (uint32_t)slot;
+            break;
+        }
+    }
+    p->off_mask = (uint32_t)p->stages * p->slot_bytes;
+    p->off_bar = (uint32_t)round_up(p->off_mask + 32u * (uint32_t)p->stages, 16);
+    p->off_outer = (uint32_t)round_up(p->off_bar + 16u * (uint32_t)p->stages, 16);
+    p->smem_bytes = p->off_outer + outer_bytes;
+
+    // Persistent CTAs over contiguous row ranges.
+    p->rows_total = (int64_t)p->n_hb * B * S;
+    int64_t ncta = (int64_t)kNumSMs * cps;
+    const int64_t by_rows = ceil_div(p->rows_total, kMinRowsPerCta);
+    if (ncta > by_rows)
+        ncta = by_rows;
+    if (ncta < 1)
+        ncta = 1;
+    p->ncta = (int32_t)ncta;
+
+    const int64_t bs = B * S;
+    for (int hb = 0; hb < p->n_hb; ++hb) {
+        p->c_lo[hb] = p->ncta;
+        p->c_hi[hb] = -1;
+    }
+    p->maxseg = 1;
+    for (int64_t c = 0; c < ncta; ++c) {
+        const int64_t r0 = cta_row_begin(c, p->rows_total, ncta);
+        const int64_t r1 = cta_row_begin(c + 1, p->rows_total, ncta);
+        const int hb0 = (int)(r0 / bs), hb1 = (int)((r1 - 1) / bs);
+        if (hb1 - hb0 + 1 > p->maxseg)
+            p->maxseg = hb1 - hb0 + 1;
+        for (int hb = hb0; hb <= hb1; ++hb) {
+            if (c < p->c_lo[hb])
+                p->c_lo[hb] = (int32_t)c;
+            if (c > p->c_hi[hb])
+                p->c_hi[hb] = (int32_t)c;
+        }
+    }
+
+    p->ws_status_off = kHeaderBytes;
+    p->ws_part_off = kHeaderBytes + (uint64_t)round_up(4 * ncta, 256);
+    p->ws_bytes = p->ws_part_off +
+                  (uint64_t)ncta * (uint64_t)p->maxseg * kW * (uint64_t)p->hb_width * 4u;
+    p->reduce_blocks = (int32_t)(p->n_hb * kW * ceil_div(p->hb_width, kReduceCols));
+    return kOk;
+}
+
+}  // namespace mcc1d

@@ -1,0 +1,85 @@
+// plan.h - shape validation and the launch plan of the backward (host only).
+//
+// The plan is a pure function of (S, B, H, dtype): the partition of the work,
+// the order of every floating-point sum and the workspace size never depend on
+// the device it later runs on, so equal inputs give bitwise-equal outputs.
+#pragma once
+
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define MCC1D_HD __host__ __device__
+#else
+#define MCC1D_HD
+#endif
+
+namespace mcc1d {
+
+constexpr int kW = 3;                 // the only kernel width the operator supports
+constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs
+constexpr int kSmemPerSM = 233472;    // 228 KB of shared memory per SM
+constexpr int kSmemPerCtaMax = 232448;// 227 KB opt-in maximum per CTA
+constexpr int kSmemReservedPerCta = 1024;
+constexpr int kMaxHb = 64;            // upper bound on H-blocks recorded in a plan
+constexpr int kMaxHbWidth = 1024;     // halves per H-block (2 KB rows)
+constexpr int kMinRowsPerCta = 64;    // below this a CTA is not worth its pipeline fill
+constexpr int kFlushStages = 16;      // stages between register -> shared accumulator flushes
+constexpr int kReduceCols = 128;      // gradWeight columns per reduce CTA (32 lanes x 4)
+constexpr int kReduceWarps = 32;      // c-splits per reduce CTA
+constexpr uint64_t kHeaderBytes = 256;
+
+// Status codes, the same values as the public header.
+enum : int32_t {
+    kOk = 0,
+    kErrNull = 161001,
+    kErrInvalid = 161002,
+    kErrShape = 561002,
+    kErrWorkspace = 561003,
+    kErrCuda = 561100,
+    kErrTimeout = 561101,
+};
+
+struct Plan {
+    int64_t S, B, H;
+    int32_t dtype;           // 0 bf16, 1 fp16
+    // H is cut into n_hb blocks of hb_width halves (the last may be narrower).
+    int32_t hb_width, n_hb;
+    // CTA shape: warp 0 produces (bulk copies), consumer_warps compute; each
+    // consumer thread owns one 16-byte vector (8 halves) of the H-block.
+    int32_t consumer_warps, threads;
+    int32_t rows_per_stage;  // R: rows of x (and R+2 of gradY) per ring slot
+    int32_t stages;          // ring slots
+    int32_t ctas_per_sm;
+    // Work: the rows (hb, j, i), flattened with i fastest, N = n_hb*B*S, are
+    // split into ncta contiguous ranges [c*N/ncta, (c+1)*N/ncta).
+    int64_t rows_total;
+    int32_t ncta;
+    int32_t maxseg;          // most H-blocks any one CTA range touches
+    int32_t c_lo[kMaxHb], c_hi[kMaxHb];  // CTAs whose range touches H-block hb
+    // Shared memory layout (bytes from the dynamic smem base).
+    uint32_t row_bytes;      // stride of one staged row = hb_width * 2
+    uint32_t slot_bytes;     // (2R + 2) rows
+    uint32_t off_mask;       // stages x 32 mask bytes
+    uint32_t off_bar;        // 2 x stages mbarriers
+    uint32_t off_outer;      // 24 fp32 accumulators per consumer thread
+    uint32_t smem_bytes;
+    // Workspace layout: header | per-CTA status words | fp32 partials
+    // [ncta][maxseg][W][hb_width].
+    uint64_t ws_status_off, ws_part_off, ws_bytes;
+    // Reduce launch.
+    int32_t reduce_blocks;
+};
+
+// Shape and dtype checks of the page's constraints. Returns kOk, kErrInvalid
+// (dtype) or kErrShape.
+int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype);
+
+// Fills *p for a valid shape; returns the validate_shape status otherwise.
+int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p);
+
+// First row of CTA c's range.
+MCC1D_HD inline int64_t cta_row_begin(int64_t c, int64_t rows_total, int64_t ncta) {
+    return c * rows_total / ncta;
+}
+
+}  // namespace mcc1d

@@ -1,0 +1,147 @@
+/*
+ * mcc1d.h - masked causal depthwise conv1d backward (W = 3) for NVIDIA GB300.
+ *
+ * C ABI of libmcc1d.so. The operation is the one defined on the CANN operator
+ * page "aclnnMaskedCausalConv1dBackward", section 功能说明 (function
+ * description), 计算公式 (formulas). With gradY, x, gradX laid out [S,B,H],
+ * weight [W,H] and the optional bool mask [B,S]:
+ *
+ *   gradYMasked(i,j,h) = mask(j,i) * gradY(i,j,h)
+ *   gradX(i,j,h)       = sum over k = 0..W-1 of gradYMasked(i+k,j,h) * weight(W-1-k,h)
+ *   gradWeight(k,h)    = sum over j < B, i < S of gradYMasked(i+W-1-k,j,h) * x(i,j,h)
+ *
+ * Terms whose S index falls outside [0,S) are zero; batches never mix; H is
+ * the depthwise (elementwise) axis. W is 3, the only width the page supports.
+ *
+ * The page's two-phase call (函数原型 / function prototypes) maps to
+ *   1. mcc1d_bwd_workspace_size: validate and size the workspace (host only);
+ *   2. mcc1d_bwd: validate again and enqueue the computation on a stream.
+ * Raw pointers carry no shapes, so the second phase takes the shape again in
+ * place of the page's opaque executor object.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no memory and keeps no state between calls.
+ *  - Tensors are dense and row-major: gradY, x, gradX [S,B,H]; weight and
+ *    gradWeight [W,H]; mask [B,S] with one byte per position, nonzero = keep.
+ *  - gradY, x, weight, gradX, gradWeight and workspace must be 16-byte
+ *    aligned; the mask may have any alignment.
+ *  - The data type (bf16 or fp16) is the same for all five 16-bit tensors, as
+ *    the page's parameter table (参数说明) requires. Accumulation is fp32;
+ *    outputs are rounded to nearest even.
+ *  - gradX and gradWeight must not overlap each other, an input or the
+ *    workspace (not checked).
+ *  - Results are deterministic: the same inputs, shape and device give
+ *    bitwise-identical outputs (the page promises a deterministic
+ *    implementation, 约束说明 / constraints). No floating-point atomics are
+ *    used; every sum has a fixed order that depends on the shape only.
+ *  - Status codes mirror the page's return codes (返回值 / return values);
+ *    codes >= 561003 are this library's own.
+ *
+ * Shape limits (约束说明 / constraints): 1 <= B <= 32, 1 <= B*S <= 524288,
+ * 384 <= H <= 24576 with H % 64 == 0, W == 3. Anything else is
+ * MCC1D_ERR_INNER_TILING_ERROR. The page also promises that inputs hold no
+ * inf or NaN and that no intermediate value overflows the 16-bit type; the
+ * library relies on that and does not check it.
+ */
+#ifndef MCC1D_H
+#define MCC1D_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of gradY, x, weight, gradX and gradWeight (the page allows
+ * BFLOAT16 and FLOAT16). */
+typedef enum { MCC1D_BF16 = 0, MCC1D_FP16 = 1 } mcc1d_dtype;
+
+typedef enum {
+    MCC1D_OK = 0,
+    /* A required pointer is null (page code ACLNN_ERR_PARAM_NULLPTR). */
+    MCC1D_ERR_PARAM_NULLPTR = 161001,
+    /* Unsupported dtype, or a tensor pointer that is not 16-byte aligned
+     * (page code ACLNN_ERR_PARAM_INVALID: dtype or format out of range). */
+    MCC1D_ERR_PARAM_INVALID = 161002,
+    /* Shape outside the supported range (page code ACLNN_ERR_INNER_TILING_ERROR). */
+    MCC1D_ERR_INNER_TILING_ERROR = 561002,
+    /* The workspace passed to mcc1d_bwd is smaller than the size phase 1 reported. */
+    MCC1D_ERR_WORKSPACE = 561003,
+    /* A CUDA runtime call failed (launch, attribute or copy); nothing is
+     * guaranteed about the outputs. */
+    MCC1D_ERR_CUDA = 561100,
+    /* Reported by mcc1d_bwd_device_status: a device-side wait of the last
+     * call gave up after its time limit and the outputs are not valid. */
+    MCC1D_ERR_DEVICE_TIMEOUT = 561101
+} mcc1d_status;
+
+/*
+ * Phase 1 (page: aclnnMaskedCausalConv1dBackwardGetWorkspaceSize).
+ *
+ * Validates the shape and dtype and writes to *bytes_out the size of device
+ * workspace that mcc1d_bwd needs for this shape. Runs on the host only and
+ * touches no device. has_mask (0 or 1) is accepted to mirror the page's
+ * optional mask; the size does not depend on it.
+ *
+ * Errors: MCC1D_ERR_PARAM_NULLPTR if bytes_out is null;
+ * MCC1D_ERR_PARAM_INVALID for an unknown dtype; MCC1D_ERR_INNER_TILING_ERROR
+ * for a shape outside the limits above. *bytes_out is untouched on error.
+ */
+int32_t mcc1d_bwd_workspace_size(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                                 int32_t has_mask, uint64_t *bytes_out);
+
+/*
+ * Phase 2 (page: aclnnMaskedCausalConv1dBackward).
+ *
+ * Enqueues the backward on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream) of the current device and returns without waiting. All
+ * tensor pointers must belong to the current device.
+ *
+ *   gradY        [S,B,H] input, dtype
+ *   x            [S,B,H] input, dtype (the forward's input)
+ *   weight       [W,H]   input, dtype
+ *   mask_or_null [B,S]   input bytes, nonzero = keep; NULL keeps every position
+ *   gradX        [S,B,H] output, dtype; every element is written
+ *   gradWeight   [W,H]   output, dtype; every element is written
+ *   workspace    device scratch of at least workspace_bytes bytes, where
+ *                workspace_bytes >= the size phase 1 reported for this shape.
+ *                Its contents on entry are ignored and are overwritten; it must
+ *                not be used by anything else until the call has completed on
+ *                the stream. Two calls that may run at the same time need two
+ *                workspaces.
+ *
+ * Returns MCC1D_OK once the work is enqueued. Errors (nothing is enqueued):
+ * MCC1D_ERR_PARAM_NULLPTR (a null tensor or workspace pointer),
+ * MCC1D_ERR_PARAM_INVALID (dtype, or a pointer not 16-byte aligned),
+ * MCC1D_ERR_INNER_TILING_ERROR (shape), MCC1D_ERR_WORKSPACE (workspace_bytes
+ * too small), MCC1D_ERR_CUDA (a launch failed; the CUDA error is left for
+ * cudaGetLastError to report).
+ */
+int32_t mcc1d_bwd(const void *gradY, const void *x, const void *weight,
+                  const uint8_t *mask_or_null, void *gradX, void *gradWeight,
+                  void *workspace, void *stream,
+                  int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                  uint64_t workspace_bytes);
+
+/*
+ * Device-side status of the last mcc1d_bwd that used `workspace`: waits for
+ * `stream` to finish, then copies the status word that the call left in the
+ * workspace to *status_out (MCC1D_OK, or MCC1D_ERR_DEVICE_TIMEOUT when a
+ * bounded device-side wait gave up). Synchronous; meant for tests and
+ * debugging. Returns MCC1D_ERR_PARAM_NULLPTR for null pointers and
+ * MCC1D_ERR_CUDA if the copy or the synchronisation failed.
+ */
+int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *status_out);
+
+/* Static text for a status code; never NULL. */
+const char *mcc1d_status_string(int32_t status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int32_t mcc1d_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MCC1D_H */

@@ -1,0 +1,107 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol,
+and rejects bad arguments with the page's status codes before touching any
+device (no GPU needed; only failing calls are made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_conv_backward_gb300 as m
+from causal_conv_backward_gb300 import build as cbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+NULLPTR, INVALID, SHAPE, WORKSPACE = 161001, 161002, 561002, 561003
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return m.load()
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(mcc1d_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "mcc1d_bwd" in names and "mcc1d_bwd_workspace_size" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def ws(S, B, H, W=3, dtype=0, has_mask=1, out=True):
+    v = ctypes.c_uint64(12345)
+    st = m.load().mcc1d_bwd_workspace_size(S, B, H, W, dtype, has_mask, ctypes.byref(v) if out else None)
+    return st, v.value
+
+
+def test_workspace_size_valid_shapes(lib):
+    for (S, B, H) in [(1, 1, 384), (64, 2, 384), (4096, 8, 2048), (524288, 1, 384),
+                      (16384, 32, 4096), (8192, 4, 24576), (16384, 32, 24576), (1, 32, 24576)]:
+        for dt in (0, 1):
+            st, n = ws(S, B, H, dtype=dt)
+            assert st == 0 and n > 0
+            assert ws(S, B, H, dtype=dt, has_mask=0) == (0, n)  # the mask does not change it
+            assert ws(S, B, H, dtype=dt) == (0, n)              # deterministic
+
+
+@pytest.mark.parametrize("S,B,H,W,dt,code", [
+    (1, 1, 384, 3, 2, INVALID), (1, 1, 384, 3, -1, INVALID),
+    (0, 1, 384, 3, 0, SHAPE), (1, 0, 384, 3, 0, SHAPE), (1, 33, 384, 3, 0, SHAPE),
+    (524289, 1, 384, 3, 0, SHAPE), (16385, 32, 384, 3, 0, SHAPE), (1, 1, 320, 3, 0, SHAPE),
+    (1, 1, 392, 3, 0, SHAPE), (1, 1, 24640, 3, 0, SHAPE), (1, 1, 384, 2, 0, SHAPE),
+    (1, 1, 384, 4, 0, SHAPE), (-5, 1, 384, 3, 0, SHAPE), (1 << 40, 1, 384, 3, 0, SHAPE),
+])
+def test_workspace_size_rejects(lib, S, B, H, W, dt, code):
+    st, v = ws(S, B, H, W, dt)
+    assert st == code and v == 12345
+
+
+def test_workspace_size_null_out(lib):
+    assert ws(64, 2, 384, out=False)[0] == NULLPTR
+
+
+def call(gy=0x1000, x=0x2000, w=0x3000, mask=None, gx=0x4000, gw=0x5000, wsp=0x6000,
+         S=64, B=2, H=384, W=3, dt=0, wsb=None):
+    if wsb is None:
+        wsb = ws(S, B, H)[1] if ws(S, B, H)[0] == 0 else 0
+    return m.load().mcc1d_bwd(gy, x, w, mask, gx, gw, wsp, None, S, B, H, W, dt, wsb)
+
+
+@pytest.mark.parametrize("which", ["gy", "x", "w", "gx", "gw", "wsp"])
+def test_bwd_null_pointer(lib, which):
+    assert call(**{which: None}) == NULLPTR
+
+
+@pytest.mark.parametrize("which", ["gy", "x", "w", "gx", "gw", "wsp"])
+def test_bwd_misaligned_pointer(lib, which):
+    base = {"gy": 0x1000, "x": 0x2000, "w": 0x3000, "gx": 0x4000, "gw": 0x5000, "wsp": 0x6000}
+    assert call(**{which: base[which] + 2}) == INVALID
+
+
+def test_bwd_bad_dtype_and_shape(lib):
+    assert call(dt=7, wsb=1 << 30) == INVALID
+    assert call(B=33, wsb=1 << 30) == SHAPE
+    assert call(H=400, wsb=1 << 30) == SHAPE
+    assert call(W=2, wsb=1 << 30) == SHAPE
+
+
+def test_bwd_workspace_too_small(lib):
+    need = ws(4096, 8, 2048)[1]
+    assert call(S=4096, B=8, H=2048, wsb=need - 1) == WORKSPACE
+
+
+def test_status_strings(lib):
+    for code in (0, NULLPTR, INVALID, SHAPE, WORKSPACE, 561100, 561101):
+        s = m.mcc1d_status_string(code)
+        assert s.startswith("MCC1D_")
+    assert m.mcc1d_status_string(42) == "unknown mcc1d status"
+    assert m.mcc1d_version() >= 100

@@ -1,0 +1,181 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+gradX: at most 1 ulp of the output type from the oracle's fp64 value rounded
+once; gradWeight: |gpu - exact| <= 1e-5 * sum|terms| + ulp(exact). Outputs
+are pre-filled with NaN patterns and the workspace with 0xFF bytes, so an
+element the kernels fail to write, or a result that depends on stale
+workspace data, cannot pass.
+"""
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from parity import GX_MAX_ULP, gradw_ratio, max_ulp, run_cuda, values
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_conv_backward_gb300 import build
+    build.build()
+
+
+def oracle_full(wl, inp):
+    return oracle.bwd(wl.S, wl.B, wl.H, wl.W, wl.dtype, inp["gy"], inp["x"], inp["w"], inp["mask"],
+                      want_exact=True)
+
+
+def check_against_oracle(wl, inp, gx, gw, status, ref=None):
+    assert status == 0
+    ref = ref or oracle_full(wl, inp)
+    ulp = max_ulp(gx, ref["gx"])
+    assert ulp <= GX_MAX_ULP, f"gradX off by {ulp} ulp"
+    ratio = gradw_ratio(gw, ref["gw_exact"], ref["gw_abs"], wl.dtype)
+    assert ratio <= 1.0, f"gradWeight error is {ratio:.3f} x tolerance"
+    return ulp, ratio
+
+
+# ------------------------------------------------------------- full workloads
+WORKLOAD_CASES = [
+    ("s64_b2_h384_bf16", True), ("s64_b2_h384_bf16", False),
+    ("s4096_b8_h2048_bf16", True),
+    ("s524288_b1_h384_bf16", True),
+    ("s8192_b4_h24576_bf16", True),
+    ("s16384_b32_h4096_fp16", True), ("s16384_b32_h4096_fp16", False),
+]
+
+
+@pytest.mark.parametrize("name,with_mask", WORKLOAD_CASES,
+                         ids=[f"{n}{'' if m else '_nomask'}" for n, m in WORKLOAD_CASES])
+def test_workload_full(name, with_mask):
+    """Every element of gradX and gradWeight at the workload's full size, in
+    the same launch configuration the benchmark times."""
+    wl = datagen.WORKLOADS[name]
+    if not with_mask:
+        wl = wl.without_mask()
+    inp = datagen.generate(wl, seed=0)
+    gx, gw, status, _ = run_cuda(inp, wl.S, wl.B, wl.H, wl.dtype)
+    ulp, ratio = check_against_oracle(wl, inp, gx, gw, status)
+    print(f"{wl.name}: gradX max {ulp} ulp, gradWeight max {ratio:.4f} x tolerance")
+
+
+# ------------------------------------------------------------- edge shapes
+EDGE = []
+for dt in ("bf16", "fp16"):
+    for S in (1, 2, 3, 4, 5, 7, 8, 9, 13, 63, 64, 65, 129):
+        EDGE.append((S, 1, 384, dt))
+    for (S, B, H) in ((1, 3, 448), (2, 2, 640), (3, 5, 1088), (17, 3, 1088), (33, 2, 2112),
+                      (5, 32, 384), (7, 32, 1024), (2, 1, 24576), (9, 2, 24576), (300, 3, 1984),
+                      (1000, 1, 384), (2049, 2, 448)):
+        EDGE.append((S, B, H, dt))
+
+
+@pytest.mark.parametrize("S,B,H,dt", EDGE, ids=[f"s{a}_b{b}_h{c}_{d}" for a, b, c, d in EDGE])
+def test_edge_shapes(S, B, H, dt):
+    """Short sequences (the two-row halo crossing the end), ragged stages,
+    ragged and multiple H-blocks, CTA ranges that cross sequences and
+    H-blocks; random mask."""
+    wl = datagen.Workload(f"edge_s{S}_b{B}_h{H}_{dt}", S, B, H, dt, mask=("bernoulli", 0.7))
+    inp = datagen.generate(wl, seed=S * 1000 + B * 10 + H)
+    gx, gw, status, _ = run_cuda(inp, S, B, H, dt)
+    check_against_oracle(wl, inp, gx, gw, status)
+
+
+def test_page_sample_zeros():
+    """The operator page's call example: S=1, B=2, H=384, fp16, every input
+    zero and a mask of zero bytes: both outputs are zero."""
+    S, B, H = 1, 2, 384
+    inp = {"gy": np.zeros((S, B, H), np.uint16), "x": np.zeros((S, B, H), np.uint16),
+           "w": np.zeros((3, H), np.uint16), "mask": np.zeros((B, S), np.uint8)}
+    gx, gw, status, _ = run_cuda(inp, S, B, H, "fp16")
+    assert status == 0
+    assert np.all(values(gx, "fp16") == 0) and np.all(values(gw, "fp16") == 0)
+
+
+# ------------------------------------------------------------- mask semantics
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_mask_all_zero_and_all_one(dt):
+    wl = datagen.Workload("m", 777, 3, 1088, dt, mask=("none",))
+    inp = datagen.generate(wl, seed=5)
+    gx0, gw0, st0, _ = run_cuda(inp, wl.S, wl.B, wl.H, dt, mask_override=np.zeros((3, 777), np.uint8))
+    assert st0 == 0 and np.all(values(gx0, dt) == 0) and np.all(values(gw0, dt) == 0)
+    gxn, gwn, _, _ = run_cuda(inp, wl.S, wl.B, wl.H, dt, mask_override=None)
+    gx1, gw1, _, _ = run_cuda(inp, wl.S, wl.B, wl.H, dt, mask_override=np.ones((3, 777), np.uint8))
+    assert np.array_equal(gx1, gxn) and np.array_equal(gw1, gwn)
+    # any nonzero byte keeps the position
+    gx2, gw2, _, _ = run_cuda(inp, wl.S, wl.B, wl.H, dt, mask_override=np.full((3, 777), 0x80, np.uint8))
+    assert np.array_equal(gx2, gxn) and np.array_equal(gw2, gwn)
+
+
+# ------------------------------------------------------------- determinism, streams
+def test_deterministic_across_runs_and_workspace_garbage():
+    """Five runs, the workspace refilled with different garbage each time:
+    bitwise-identical outputs."""
+    wl = datagen.WORKLOADS["s4096_b8_h2048_bf16"]
+    inp = datagen.generate(wl, seed=1)
+    ws = None
+    first = None
+    for r in range(5):
+        if ws is not None:
+            ws.fill_(0x7F if r % 2 else 0xFF)
+        gx, gw, status, ws = run_cuda(inp, wl.S, wl.B, wl.H, wl.dtype, workspace=ws)
+        assert status == 0
+        if first is None:
+            first = (gx, gw)
+        else:
+            assert np.array_equal(gx, first[0]) and np.array_equal(gw, first[1])
+
+
+def test_side_stream_matches_default_stream():
+    wl = datagen.WORKLOADS["s524288_b1_h384_bf16"].resized(S=65536)
+    inp = datagen.generate(wl, seed=2)
+    gx_a, gw_a, _, _ = run_cuda(inp, wl.S, wl.B, wl.H, wl.dtype)
+    s = torch.cuda.Stream()
+    gx_b, gw_b, st, _ = run_cuda(inp, wl.S, wl.B, wl.H, wl.dtype, stream=s)
+    assert st == 0 and np.array_equal(gx_a, gx_b) and np.array_equal(gw_a, gw_b)
+
+
+# ------------------------------------------------------------- maximum size
+def test_max_size_property():
+    """B*S = 524288 tokens (B = 32) and H = 24576, the largest shape the page
+    allows, bf16. With gradY = x = 1 and small integer weights every value is
+    an exact small integer, so gradX(i,j,h) = sum_k mask(j,i+k) * w(2-k,h) and
+    gradWeight(k,h) = count of kept positions i+2-k < S, known in closed form
+    from the mask; checked for every element on the device."""
+    import causal_conv_backward_gb300 as m
+    S, B, H, dt = 16384, 32, 24576, "bf16"
+    dev = "cuda"
+    gen = torch.Generator(device="cpu").manual_seed(0)
+    mask = (torch.rand((B, S), generator=gen) < 0.9).to(torch.uint8)
+    wv = (torch.arange(3 * H, dtype=torch.int64).reshape(3, H) * 7 % 5 - 2).to(torch.float32)
+    one = torch.ones((S, B, H), dtype=torch.bfloat16, device=dev)
+    gy, x = one, one  # read-only inputs may alias
+    w = wv.to(torch.bfloat16).to(dev)
+    md = mask.to(dev)
+    gx = torch.empty((S, B, H), dtype=torch.bfloat16, device=dev)
+    gw = torch.empty((3, H), dtype=torch.bfloat16, device=dev)
+    nbytes = m.mcc1d_bwd_workspace_size(S, B, H, 3, dt, True)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=dev)
+    m.mcc1d_bwd(gy, x, w, md, gx, gw, ws, torch.cuda.current_stream(), S, B, H, 3, 0, nbytes)
+    assert m.mcc1d_bwd_device_status(ws, torch.cuda.current_stream()) == 0
+    # gYm(i,j) = mask(j,i); shifted copies with zero padding past S
+    mt = md.t().to(torch.float32)                 # [S,B]
+    sh = [torch.zeros_like(mt) for _ in range(3)]
+    for k in range(3):
+        sh[k][: S - k] = mt[k:]
+    wd = w.to(torch.float32)
+    for s0 in range(0, S, 2048):
+        sl = slice(s0, min(S, s0 + 2048))
+        exp = (sh[0][sl, :, None] * wd[2] + sh[1][sl, :, None] * wd[1] + sh[2][sl, :, None] * wd[0])
+        assert torch.equal(gx[sl].to(torch.float32), exp), f"rows {sl}"
+    counts = torch.stack([sh[2 - k].sum() for k in range(3)]).to(torch.float64).cpu().numpy()
+    exp_w = np.broadcast_to(counts[:, None], (3, H))
+    got_w = gw.to(torch.float32).cpu().numpy().astype(np.float64)
+    ref_bits = oracle.encode(exp_w[:, :1], "bf16")
+    assert np.all(got_w == values(ref_bits, "bf16")), (got_w[:, 0], exp_w[:, 0])
