@@ -632,8 +632,9 @@ static bool ensure_smem_attr(const void *fn, int slot_id)
     const uint64_t bit = 1ull << (dev & 63);
     if (done[slot_id].load(std::memory_order_acquire) & bit)
         return true;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCtaMax) !=
-        cudaSuccess)
+    // leave room for the kernel's few bytes of static shared memory
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemPerCtaMax - 1024) != cudaSuccess)
         return false;
     done[slot_id].fetch_or(bit, std::memory_order_acq_rel);
     return true;
