@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-mask", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="run on the first N positions of the workload (small profiling captures)")
     return ap.parse_args(argv)
 
 
@@ -149,6 +151,13 @@ def workload(name: str, no_mask: bool):
     return wl.without_mask() if no_mask else wl
 
 
+def chosen_workload(args):
+    wl = workload(args.workload, args.no_mask)
+    if args.seq_len:
+        wl = wl.resized(S=args.seq_len)
+    return wl
+
+
 def describe(wl) -> dict:
     mask = "none" if wl.mask[0] == "none" else "(" + ",".join(str(v) for v in wl.mask) + ")"
     return {"workload": wl.name, "S": wl.S, "B": wl.B, "H": wl.H, "W": wl.W, "io_dtype": wl.dtype,
@@ -230,7 +239,7 @@ def gpu_arm(args):
     cbuild.build()
     m.load()
 
-    wl = workload(args.workload, args.no_mask)
+    wl = chosen_workload(args)
     code = m.dtype_code(wl.dtype)
 
     def pinned(shape, dt):
@@ -357,7 +366,7 @@ def reference_arm(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    wl = workload(args.workload, args.no_mask)
+    wl = chosen_workload(args)
     K = args.steps
     t, sample, nt = time_oracle(wl, REF_SAMPLE_S, steps=K, warmup=max(0, args.warmup))
     value = sample.algorithmic_bytes() / t / 1e9

@@ -318,6 +318,22 @@ def pin_torch_autograd(orc):
                 assert np.array_equal(r["gx"][same], tgx[same].astype(np.float16).view(np.uint16))
 
 
+def pin_forward_torch(orc):
+    """The implied forward y = mask * causal depthwise conv(x, w) equals
+    torch's float64 conv1d (left padding W-1, groups = H) on the CPU."""
+    rng = np.random.default_rng(41)
+    for dt in ("bf16", "fp16"):
+        for (S, B, H, W) in ((1, 2, 3, 3), (6, 2, 5, 3), (40, 3, 7, 3), (9, 1, 4, 5)):
+            x, w = rand_bits(rng, (S, B, H), dt), rand_bits(rng, (W, H), dt)
+            mask = (rng.random((B, S)) < 0.7).astype(np.uint8)
+            y = orc.fwd(S, B, H, W, dt, x, w, mask)
+            xt = torch.tensor(dec(x, dt)).permute(1, 2, 0)
+            wt = torch.tensor(dec(w, dt)).t().contiguous().unsqueeze(1)
+            yt = torch.nn.functional.conv1d(torch.nn.functional.pad(xt, (W - 1, 0)), wt, groups=H)
+            yt = (yt * torch.tensor(mask != 0, dtype=torch.float64)[:, None, :]).permute(2, 0, 1).numpy()
+            assert np.allclose(y, yt, rtol=0, atol=1e-12 * (np.abs(yt).max() + 1)), (dt, S, B, H, W)
+
+
 # ---------------------------------------------------------------- conversions
 def pin_converters(orc):
     """Decoding every 16-bit pattern, and rounding doubles to 16 bits (ties to
@@ -371,4 +387,4 @@ def pin_gradx_at(orc):
 
 ALL_PINS = [pin_golden, pin_closed_form_ones, pin_shift_identities, pin_mask_special_cases,
             pin_s1, pin_batch_independence, pin_jacobian_bruteforce, pin_adjoint_identity,
-            pin_torch_autograd, pin_converters, pin_gradx_at]
+            pin_torch_autograd, pin_forward_torch, pin_converters, pin_gradx_at]

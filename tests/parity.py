@@ -65,8 +65,11 @@ def to_device(bits: np.ndarray, dtype: str, device="cuda"):
     return t.view(getattr(torch, TORCH_DT[dtype]))
 
 
+_KEEP = object()
+
+
 def run_cuda(inp: dict, S, B, H, dtype, *, W=3, stream=None, workspace=None, fill_outputs=True,
-             mask_override="keep"):
+             mask_override=_KEEP):
     """Run the CUDA path once through the C ABI; returns (gx_bits, gw_bits,
     device_status, workspace). Outputs are pre-filled with NaN patterns so an
     unwritten element cannot pass."""
@@ -76,7 +79,7 @@ def run_cuda(inp: dict, S, B, H, dtype, *, W=3, stream=None, workspace=None, fil
     gy = to_device(inp["gy"], dtype)
     x = to_device(inp["x"], dtype)
     w = to_device(inp["w"], dtype)
-    mask = inp["mask"] if mask_override == "keep" else mask_override
+    mask = inp["mask"] if mask_override is _KEEP else mask_override
     md = None if mask is None else torch.from_numpy(np.ascontiguousarray(mask)).cuda()
     gx = torch.empty_like(gy)
     gw = torch.empty_like(w)
