@@ -48,6 +48,8 @@ def load():
         lib.mcc1d_bwd_workspace_size.restype = i32
         lib.mcc1d_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, u64]
         lib.mcc1d_bwd.restype = i32
+        lib.mcc1d_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32]
+        lib.mcc1d_bwd_noalloc.restype = i32
         lib.mcc1d_bwd_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
         lib.mcc1d_bwd_device_status.restype = i32
         lib.mcc1d_status_string.argtypes = [i32]
@@ -93,6 +95,22 @@ def mcc1d_bwd(gradY, x, weight, mask_or_null, gradX, gradWeight, workspace, stre
                           dtype_code(dtype), int(workspace_bytes))
     if st != 0:
         raise Mcc1dError(st, "mcc1d_bwd")
+
+
+def mcc1d_bwd_noalloc(gradY, x, weight, mask_or_null, gradX, gradWeight, stream,
+                      S, B, H, W, dtype) -> None:
+    """Enqueue the backward with the library's fixed scratch array instead of a
+    workspace (for callers that cannot allocate device memory)."""
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = load().mcc1d_bwd_noalloc(_ptr(gradY), _ptr(x), _ptr(weight), _ptr(mask_or_null),
+                                  _ptr(gradX), _ptr(gradWeight), stream or None, S, B, H, W,
+                                  dtype_code(dtype))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_bwd_noalloc")
+
+
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
 def mcc1d_bwd_device_status(workspace, stream=None) -> int:

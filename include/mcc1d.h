@@ -134,6 +134,43 @@ int32_t mcc1d_bwd(const void *gradY, const void *x, const void *weight,
  */
 int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *status_out);
 
+/*
+ * Backward without a workspace argument. The operator page has no
+ * counterpart to this call: it is for callers that cannot allocate device
+ * memory at call time (code running inside a runtime or framework that owns
+ * every device allocation, or whose memory budget is fixed to the tensors it
+ * is handed) and so cannot supply the workspace that mcc1d_bwd needs.
+ *
+ * Arguments and results are those of mcc1d_bwd without workspace and
+ * workspace_bytes; the call allocates nothing. Its scratch (the per-CTA
+ * gradWeight partial sums and status words) lives instead in one fixed
+ * device array of MCC1D_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library
+ * image, which every GPU that loads the library holds until the process
+ * exits.
+ *
+ *  - A shape whose mcc1d_bwd_workspace_size exceeds MCC1D_NOALLOC_SCRATCH_BYTES
+ *    is rejected with MCC1D_ERR_WORKSPACE before anything is enqueued. Every
+ *    shape within the limits above needs at most about 7.5 MB, so all of them
+ *    fit; the check guards against a future plan needing more.
+ *  - All calls on a device share the one array. Calls that may overlap on the
+ *    GPU (different streams, or host threads with no ordering between them)
+ *    race on it and give wrong results: order them on one stream or with
+ *    events.
+ *  - The array keeps what the last call left in it; the kernels write every
+ *    scratch word before they read it, so nothing needs clearing between calls.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture begins.
+ *  - mcc1d_bwd_device_status does not apply to this call.
+ * Errors: as mcc1d_bwd, plus MCC1D_ERR_WORKSPACE for a shape too large for the
+ * array and MCC1D_ERR_CUDA if the address lookup fails.
+ */
+#define MCC1D_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+int32_t mcc1d_bwd_noalloc(const void *gradY, const void *x, const void *weight,
+                          const uint8_t *mask_or_null, void *gradX, void *gradWeight,
+                          void *stream, int64_t S, int64_t B, int64_t H, int64_t W,
+                          int32_t dtype);
+
 /* Static text for a status code; never NULL. */
 const char *mcc1d_status_string(int32_t status);
 
