@@ -25,8 +25,8 @@
 //   fp32. Each CTA writes one fp32 partial [3][H-block] per H-block it
 //   touched into the workspace.
 // mcc1d_bwd_reduce (programmatic dependent launch):
-//   Sums the partials of every gradWeight column in a fixed order (32 serial
-//   splits over the CTAs, then a pairwise tree), rounds once to the 16-bit
+//   Sums the partials of every gradWeight column in a fixed order (64 serial
+//   slices over the CTAs, then a pairwise tree), rounds once to the 16-bit
 //   type and folds the CTAs' status words into the workspace header.
 //
 // Every device-side wait is bounded (kWaitLimitNs); a CTA whose wait gives up
@@ -53,11 +53,12 @@ struct MainParams {
     const uint16_t *w;     // [3,H]
     const uint8_t *mask;   // [B,S] or null
     uint8_t *gx;           // [S,B,H]
-    float *part;           // [ncta][maxseg][3][hb_width]
+    float *part;           // [nslots][3][hb_width]
     int32_t *status;       // [ncta]
     int64_t S, BS, H, N;
-    int32_t B, hb_width, ncta, maxseg, stages;
+    int32_t B, hb_width, ncta, stages;
     uint32_t row_bytes, slot_bytes, off_mask, off_bar, off_outer;
+    int32_t c_lo[kMaxHb], slot_base[kMaxHb];
 };
 
 struct ReduceParams {
@@ -65,9 +66,9 @@ struct ReduceParams {
     const int32_t *status;
     int32_t *header;
     uint8_t *gw;           // [3,H]
-    int64_t N, BS, H;
-    int32_t hb_width, ncta, maxseg, nchunk;
-    int32_t c_lo[kMaxHb], c_hi[kMaxHb];
+    int64_t H;
+    int32_t hb_width, ncta, nchunk;
+    int32_t c_lo[kMaxHb], c_hi[kMaxHb], slot_base[kMaxHb];
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -359,7 +360,6 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 
     Cursor cur;
     cur.init(r0, r1, p.S, p.BS);
-    const int hb_first = cur.hb;
     int hb_cur = -1;
     bool active = false;
     V8 w0, w1, w2;
@@ -382,8 +382,8 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     // the accumulators. Sum order: shared-memory level, then register level.
     auto flush_partial = [&]() {
         if (active) {
-            float *dst = p.part +
-                         (((int64_t)c * p.maxseg + (hb_cur - hb_first)) * 3) * p.hb_width + 8 * ct;
+            const int64_t slot = p.slot_base[hb_cur] + (c - p.c_lo[hb_cur]);
+            float *dst = p.part + slot * 3 * p.hb_width + 8 * ct;
 #pragma unroll
             for (int k = 0; k < 3; ++k) {
                 float v[8];
@@ -531,9 +531,6 @@ __global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_const
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
-    // Let the reduce kernel's CTAs be scheduled as this grid retires; it
-    // waits for this grid's completion before touching the partials.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int lane = threadIdx.x & 31;
     bool dead;
@@ -546,14 +543,20 @@ __global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_const
     __syncthreads();
     if (threadIdx.x == 0)
         p.status[c] = s_err ? kErrTimeout : kOk;
+    // Only now let the reduce kernel be scheduled: every partial and status
+    // word of this CTA is written and fenced before the trigger. (The reduce
+    // also waits for this grid's completion before it reads them.)
+    __threadfence();
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kReduceWarps * 32) mcc1d_bwd_reduce(const __grid_constant__ ReduceParams p)
+__global__ void __launch_bounds__(kReduceSplits * kReduceLanes) mcc1d_bwd_reduce(const __grid_constant__ ReduceParams p)
 {
-    __shared__ float4 red[kReduceWarps][32];
+    __shared__ float4 red[kReduceSplits][kReduceLanes];
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x % kReduceLanes, split = threadIdx.x / kReduceLanes;
     const int b = blockIdx.x;
     const int chunk = b % p.nchunk;
     const int k = (b / p.nchunk) % 3;
@@ -561,37 +564,41 @@ __global__ void __launch_bounds__(kReduceWarps * 32) mcc1d_bwd_reduce(const __gr
     const int64_t hb0 = (int64_t)hb * p.hb_width;
     const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
     const int col = chunk * kReduceCols + 4 * lane;
-    const int clo = p.c_lo[hb], nc = p.c_hi[hb] - p.c_lo[hb] + 1;
-    const int cb = clo + (int)((int64_t)warp * nc / kReduceWarps);
-    const int ce = clo + (int)((int64_t)(warp + 1) * nc / kReduceWarps);
+    // The H-block's partials are the contiguous slots [base, base + n);
+    // split s sums the slice [s*n/S, (s+1)*n/S) in order.
+    const int n = p.c_hi[hb] - p.c_lo[hb] + 1;
+    const int sb = (int)((int64_t)split * n / kReduceSplits);
+    const int se = (int)((int64_t)(split + 1) * n / kReduceSplits);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (col < width) {
-        for (int cc = cb; cc < ce; ++cc) {
-            const int seg = hb - (int)(cta_row_begin(cc, p.N, p.ncta) / p.BS);
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(
-                p.part + (((int64_t)cc * p.maxseg + seg) * 3 + k) * p.hb_width + col));
+        const float *src = p.part + (((int64_t)p.slot_base[hb] + sb) * 3 + k) * p.hb_width + col;
+        const int64_t step = 3 * (int64_t)p.hb_width;
+#pragma unroll 4
+        for (int q = sb; q < se; ++q, src += step) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(src));
             acc.x += v.x;
             acc.y += v.y;
             acc.z += v.z;
             acc.w += v.w;
         }
     }
-    red[warp][lane] = acc;
+    red[split][lane] = acc;
     __syncthreads();
+    // Fixed pairwise tree over the splits.
 #pragma unroll
-    for (int s = kReduceWarps / 2; s >= 1; s >>= 1) {
-        if (warp < s) {
-            float4 a = red[warp][lane];
-            const float4 o = red[warp + s][lane];
+    for (int s = kReduceSplits / 2; s >= 1; s >>= 1) {
+        if (split < s) {
+            float4 a = red[split][lane];
+            const float4 o = red[split + s][lane];
             a.x += o.x;
             a.y += o.y;
             a.z += o.z;
             a.w += o.w;
-            red[warp][lane] = a;
+            red[split][lane] = a;
         }
         __syncthreads();
     }
-    if (warp == 0 && col < width) {
+    if (split == 0 && col < width) {
         const float4 a = red[0][lane];
         const uint32_t lo = pack2<DT>(make_float2(a.x, a.y));
         const uint32_t hi = pack2<DT>(make_float2(a.z, a.w));
@@ -660,29 +667,30 @@ int32_t launch_bwd(const Plan &pl, const void *gradY, const void *x, const void 
     mp.B = (int32_t)pl.B;
     mp.hb_width = pl.hb_width;
     mp.ncta = pl.ncta;
-    mp.maxseg = pl.maxseg;
     mp.stages = pl.stages;
     mp.row_bytes = pl.row_bytes;
     mp.slot_bytes = pl.slot_bytes;
     mp.off_mask = pl.off_mask;
     mp.off_bar = pl.off_bar;
     mp.off_outer = pl.off_outer;
+    for (int h = 0; h < kMaxHb; ++h) {
+        mp.c_lo[h] = pl.c_lo[h];
+        mp.slot_base[h] = pl.slot_base[h];
+    }
 
     ReduceParams rp;
     rp.part = mp.part;
     rp.status = mp.status;
     rp.header = reinterpret_cast<int32_t *>(ws);
     rp.gw = static_cast<uint8_t *>(gradWeight);
-    rp.N = pl.rows_total;
-    rp.BS = pl.B * pl.S;
     rp.H = pl.H;
     rp.hb_width = pl.hb_width;
     rp.ncta = pl.ncta;
-    rp.maxseg = pl.maxseg;
     rp.nchunk = (pl.hb_width + kReduceCols - 1) / kReduceCols;
     for (int h = 0; h < kMaxHb; ++h) {
         rp.c_lo[h] = pl.c_lo[h];
         rp.c_hi[h] = pl.c_hi[h];
+        rp.slot_base[h] = pl.slot_base[h];
     }
 
     const int R = pl.rows_per_stage;
@@ -707,7 +715,7 @@ int32_t launch_bwd(const Plan &pl, const void *gradY, const void *x, const void 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg = {};
     rcfg.gridDim = dim3((unsigned)pl.reduce_blocks);
-    rcfg.blockDim = dim3(kReduceWarps * 32);
+    rcfg.blockDim = dim3(kReduceSplits * kReduceLanes);
     rcfg.dynamicSmemBytes = 0;
     rcfg.stream = stream;
     rcfg.attrs = attr;

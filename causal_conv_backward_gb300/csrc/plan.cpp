@@ -92,13 +92,10 @@ int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Pla
         p->c_lo[hb] = p->ncta;
         p->c_hi[hb] = -1;
     }
-    p->maxseg = 1;
     for (int64_t c = 0; c < ncta; ++c) {
         const int64_t r0 = cta_row_begin(c, p->rows_total, ncta);
         const int64_t r1 = cta_row_begin(c + 1, p->rows_total, ncta);
         const int hb0 = (int)(r0 / bs), hb1 = (int)((r1 - 1) / bs);
-        if (hb1 - hb0 + 1 > p->maxseg)
-            p->maxseg = hb1 - hb0 + 1;
         for (int hb = hb0; hb <= hb1; ++hb) {
             if (c < p->c_lo[hb])
                 p->c_lo[hb] = (int32_t)c;
@@ -107,10 +104,15 @@ int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Pla
         }
     }
 
+    p->nslots = 0;
+    for (int hb = 0; hb < p->n_hb; ++hb) {
+        p->slot_base[hb] = p->nslots;
+        p->nslots += p->c_hi[hb] - p->c_lo[hb] + 1;
+    }
+
     p->ws_status_off = kHeaderBytes;
     p->ws_part_off = kHeaderBytes + (uint64_t)round_up(4 * ncta, 256);
-    p->ws_bytes = p->ws_part_off +
-                  (uint64_t)ncta * (uint64_t)p->maxseg * kW * (uint64_t)p->hb_width * 4u;
+    p->ws_bytes = p->ws_part_off + (uint64_t)p->nslots * kW * (uint64_t)p->hb_width * 4u;
     p->reduce_blocks = (int32_t)(p->n_hb * kW * ceil_div(p->hb_width, kReduceCols));
     return kOk;
 }

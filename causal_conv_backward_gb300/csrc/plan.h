@@ -22,10 +22,11 @@ constexpr int kSmemPerCtaMax = 232448;// 227 KB opt-in maximum per CTA
 constexpr int kSmemReservedPerCta = 1024;
 constexpr int kMaxHb = 64;            // upper bound on H-blocks recorded in a plan
 constexpr int kMaxHbWidth = 1024;     // halves per H-block (2 KB rows)
-constexpr int kMinRowsPerCta = 64;    // below this a CTA is not worth its pipeline fill
+constexpr int kMinRowsPerCta = 16;    // below this a CTA is not worth its pipeline fill
 constexpr int kFlushStages = 16;      // stages between register -> shared accumulator flushes
-constexpr int kReduceCols = 128;      // gradWeight columns per reduce CTA (32 lanes x 4)
-constexpr int kReduceWarps = 32;      // c-splits per reduce CTA
+constexpr int kReduceLanes = 8;       // float4 column groups per reduce CTA (32 columns)
+constexpr int kReduceCols = 4 * kReduceLanes;
+constexpr int kReduceSplits = 64;     // contiguous slices of a column's partials per reduce CTA
 constexpr uint64_t kHeaderBytes = 256;
 
 // Status codes, the same values as the public header.
@@ -54,8 +55,11 @@ struct Plan {
     // split into ncta contiguous ranges [c*N/ncta, (c+1)*N/ncta).
     int64_t rows_total;
     int32_t ncta;
-    int32_t maxseg;          // most H-blocks any one CTA range touches
     int32_t c_lo[kMaxHb], c_hi[kMaxHb];  // CTAs whose range touches H-block hb
+    // Partial slots: CTA c's partial for H-block hb is slot
+    // slot_base[hb] + c - c_lo[hb]; the slots of one H-block are contiguous.
+    int32_t slot_base[kMaxHb];
+    int32_t nslots;
     // Shared memory layout (bytes from the dynamic smem base).
     uint32_t row_bytes;      // stride of one staged row = hb_width * 2
     uint32_t slot_bytes;     // (2R + 2) rows
@@ -64,7 +68,7 @@ struct Plan {
     uint32_t off_outer;      // 24 fp32 accumulators per consumer thread
     uint32_t smem_bytes;
     // Workspace layout: header | per-CTA status words | fp32 partials
-    // [ncta][maxseg][W][hb_width].
+    // [nslots][W][hb_width].
     uint64_t ws_status_off, ws_part_off, ws_bytes;
     // Reduce launch.
     int32_t reduce_blocks;
