@@ -18,7 +18,8 @@
 //   the R rows of gradY two positions ahead (plus the first two rows when a
 //   sequence starts) into a ring slot with cp.async.bulk, completing on the
 //   slot's "full" mbarrier; it also stores the stage's mask bytes in the slot.
-//   The consumer warps own one 16-byte vector (8 channels) each, keep the last
+//   The consumer warps own one 16-byte vector (8 channels) each (8 bytes,
+//   4 channels, when that fills the warps better, as for H = 384), keep the last
 //   two masked gradY rows in registers, and per row form gradX with a
 //   compensated three-term sum (exact fp32 products + TwoSum), store it with
 //   a streaming 16-byte store, and accumulate the three gradWeight taps in
@@ -155,9 +156,16 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b)
 }
 
 // ------------------------------------------------------------------ 16-bit types
-// DT 0 = bf16, 1 = fp16. Eight channels travel as one uint4 (16 bytes).
-struct V8 {
-    float2 e[4];
+// DT 0 = bf16, 1 = fp16. A consumer thread owns 2*NP channels: NP = 4 moves
+// 16 bytes per row (uint4), NP = 2 moves 8 bytes (uint2).
+template <int NP>
+struct Vf {
+    float2 e[NP];
+};
+
+template <int NP>
+struct Raw {
+    uint32_t u[NP];
 };
 
 template <int DT>
@@ -195,29 +203,75 @@ __device__ __forceinline__ uint32_t pack2(float2 v)
     }
 }
 
-template <int DT>
-__device__ __forceinline__ V8 unpack8(uint4 u)
+// Plain vector load (shared or global memory).
+template <int NP>
+__device__ __forceinline__ Raw<NP> load_raw(const void *p)
 {
-    V8 v;
-    v.e[0] = unpack2<DT>(u.x);
-    v.e[1] = unpack2<DT>(u.y);
-    v.e[2] = unpack2<DT>(u.z);
-    v.e[3] = unpack2<DT>(u.w);
+    Raw<NP> r;
+    if (NP == 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        r.u[0] = v.x;
+        r.u[1] = v.y;
+        r.u[2] = v.z;
+        r.u[3] = v.w;
+    } else {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        r.u[0] = v.x;
+        r.u[1] = v.y;
+    }
+    return r;
+}
+
+// Read-only global load through the non-coherent path.
+template <int NP>
+__device__ __forceinline__ Raw<NP> ldg_raw(const void *p)
+{
+    Raw<NP> r;
+    if (NP == 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+        r.u[0] = v.x;
+        r.u[1] = v.y;
+        r.u[2] = v.z;
+        r.u[3] = v.w;
+    } else {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+        r.u[0] = v.x;
+        r.u[1] = v.y;
+    }
+    return r;
+}
+
+// Streaming (evict-first) global store.
+template <int NP>
+__device__ __forceinline__ void store_cs(void *p, const uint32_t (&u)[NP])
+{
+    if (NP == 4)
+        __stcs(reinterpret_cast<uint4 *>(p), make_uint4(u[0], u[1], u[2], u[3]));
+    else
+        __stcs(reinterpret_cast<uint2 *>(p), make_uint2(u[0], u[1]));
+}
+
+template <int DT, int NP>
+__device__ __forceinline__ Vf<NP> unpack(const Raw<NP> &r)
+{
+    Vf<NP> v;
+#pragma unroll
+    for (int e = 0; e < NP; ++e)
+        v.e[e] = unpack2<DT>(r.u[e]);
     return v;
 }
 
 // A staged gradY row, masked by clearing the bits (exact +0 whatever the
 // staged bytes hold; rows past the end of S carry a zero mask byte).
-template <int DT>
-__device__ __forceinline__ V8 load_masked(const uint8_t *p, uint8_t keep_byte)
+template <int DT, int NP>
+__device__ __forceinline__ Vf<NP> load_masked(const uint8_t *p, uint8_t keep_byte)
 {
-    uint4 u = *reinterpret_cast<const uint4 *>(p);
+    Raw<NP> r = load_raw<NP>(p);
     const uint32_t keep = 0u - (uint32_t)keep_byte;
-    u.x &= keep;
-    u.y &= keep;
-    u.z &= keep;
-    u.w &= keep;
-    return unpack8<DT>(u);
+#pragma unroll
+    for (int e = 0; e < NP; ++e)
+        r.u[e] &= keep;
+    return unpack<DT, NP>(r);
 }
 
 // ------------------------------------------------------------------ row cursor
@@ -280,6 +334,7 @@ __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
     const uint32_t ring0 = smem_u32(smem);
     const int64_t row_elems = (int64_t)p.B * p.H;  // elements between rows i and i+1
+    const bool contiguous = p.B == 1 && p.H == p.hb_width;
 
     Cursor cur;
     cur.init(r0, r1, p.S, p.BS);
@@ -318,7 +373,17 @@ __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
             mbar_arrive_expect_tx(bar_full0 + 8u * slot, (uint32_t)(nG + n) * wbytes);
         __syncwarp();
         const uint32_t slot_base = ring0 + (uint32_t)slot * p.slot_bytes;
-        if (lane < nG) {
+        if (contiguous) {
+            // B = 1 and one H-block: the stage's rows are adjacent both in
+            // memory and in the slot, so one copy per tensor moves them.
+            if (lane == 0) {
+                if (nG > 0)
+                    bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.gy + 2 * (cur.i + q0) * p.H,
+                             (uint32_t)nG * wbytes, bar_full0 + 8u * slot);
+                bulk_g2s(slot_base + (uint32_t)(R + 2) * p.row_bytes, p.x + 2 * cur.i * p.H,
+                         (uint32_t)n * wbytes, bar_full0 + 8u * slot);
+            }
+        } else if (lane < nG) {
             const int q = q0 + lane;
             const int64_t e = ((cur.i + q) * p.B + cur.j) * p.H + hb0;
             bulk_g2s(slot_base + (uint32_t)q * p.row_bytes, p.gy + 2 * e, wbytes, bar_full0 + 8u * slot);
@@ -347,14 +412,15 @@ __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 }
 
 // ------------------------------------------------------------------ consumers
-template <int DT, int R>
+template <int DT, int R, int NP>
 __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t r1, int ct, int lane)
 {
     const int NS = p.stages;
     const int nct = (int)blockDim.x - 32;
     const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
-    float *outer = reinterpret_cast<float *>(smem + p.off_outer);  // [24][nct]
+    constexpr int CH = 2 * NP;                                     // channels per thread
+    float *outer = reinterpret_cast<float *>(smem + p.off_outer);  // [3*CH][nct]
     const int64_t row_stride = 2 * (int64_t)p.B * p.H;             // bytes from row i to i+1
     const int c = blockIdx.x;
 
@@ -362,20 +428,20 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     cur.init(r0, r1, p.S, p.BS);
     int hb_cur = -1;
     bool active = false;
-    V8 w0, w1, w2;
-    float2 mid[3][4];
+    Vf<NP> w0, w1, w2;
+    float2 mid[3][NP];
 #pragma unroll
     for (int k = 0; k < 3; ++k)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
+        for (int e = 0; e < NP; ++e)
             mid[k][e] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < 24; ++q)
+    for (int q = 0; q < 3 * CH; ++q)
         outer[q * nct + ct] = 0.f;
     int since_flush = 0;
-    V8 g0, g1;
+    Vf<NP> g0, g1;
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+    for (int e = 0; e < NP; ++e)
         g0.e[e] = g1.e[e] = make_float2(0.f, 0.f);
 
     // Writes this thread's share of the partial for H-block hb_cur and clears
@@ -383,27 +449,28 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     auto flush_partial = [&]() {
         if (active) {
             const int64_t slot = p.slot_base[hb_cur] + (c - p.c_lo[hb_cur]);
-            float *dst = p.part + slot * 3 * p.hb_width + 8 * ct;
+            float *dst = p.part + slot * 3 * p.hb_width + CH * ct;
 #pragma unroll
             for (int k = 0; k < 3; ++k) {
-                float v[8];
+                float v[CH];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[2 * e] = outer[(k * 8 + 2 * e) * nct + ct] + mid[k][e].x;
-                    v[2 * e + 1] = outer[(k * 8 + 2 * e + 1) * nct + ct] + mid[k][e].y;
+                for (int e = 0; e < NP; ++e) {
+                    v[2 * e] = outer[(k * CH + 2 * e) * nct + ct] + mid[k][e].x;
+                    v[2 * e + 1] = outer[(k * CH + 2 * e + 1) * nct + ct] + mid[k][e].y;
                 }
                 float4 *d4 = reinterpret_cast<float4 *>(dst + (int64_t)k * p.hb_width);
-                d4[0] = make_float4(v[0], v[1], v[2], v[3]);
-                d4[1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+                for (int q = 0; q < CH / 4; ++q)
+                    d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
 #pragma unroll
         for (int k = 0; k < 3; ++k)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
+            for (int e = 0; e < NP; ++e)
                 mid[k][e] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < 24; ++q)
+        for (int q = 0; q < 3 * CH; ++q)
             outer[q * nct + ct] = 0.f;
         since_flush = 0;
     };
@@ -420,76 +487,87 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
             hb_cur = cur.hb;
             const int64_t hb0 = (int64_t)hb_cur * p.hb_width;
             const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
-            active = 8 * ct < width;
+            active = CH * ct < width;
             if (active) {
-                w0 = unpack8<DT>(__ldg(reinterpret_cast<const uint4 *>(p.w + 0 * p.H + hb0 + 8 * ct)));
-                w1 = unpack8<DT>(__ldg(reinterpret_cast<const uint4 *>(p.w + 1 * p.H + hb0 + 8 * ct)));
-                w2 = unpack8<DT>(__ldg(reinterpret_cast<const uint4 *>(p.w + 2 * p.H + hb0 + 8 * ct)));
+                w0 = unpack<DT, NP>(ldg_raw<NP>(p.w + 0 * p.H + hb0 + CH * ct));
+                w1 = unpack<DT, NP>(ldg_raw<NP>(p.w + 1 * p.H + hb0 + CH * ct));
+                w2 = unpack<DT, NP>(ldg_raw<NP>(p.w + 2 * p.H + hb0 + CH * ct));
             }
         }
         if (!dead) {
-            const bool ok = mbar_wait_bounded(bar_full0 + 8u * slot, ph);
+            const uint32_t bar = bar_full0 + 8u * slot;
+            const bool ok = mbar_try_wait(bar, ph) || mbar_wait_bounded(bar, ph);
             dead = __any_sync(0xFFFFFFFFu, !ok);
         }
         if (!dead && active) {
-            const uint8_t *sl = smem + (size_t)slot * p.slot_bytes + 16 * ct;
+            const uint8_t *sl = smem + (size_t)slot * p.slot_bytes + 2 * CH * ct;
             const uint8_t *gys = sl;                              // gradY slot rows 0..R+1
             const uint8_t *xs = sl + (size_t)(R + 2) * p.row_bytes;  // x slot rows 0..R-1
             const uint8_t *ms = smem + p.off_mask + 32u * slot;
             if (head) {
-                g0 = load_masked<DT>(gys, ms[0]);
-                g1 = load_masked<DT>(gys + p.row_bytes, ms[1]);
+                g0 = load_masked<DT, NP>(gys, ms[0]);
+                g1 = load_masked<DT, NP>(gys + p.row_bytes, ms[1]);
             }
-            uint8_t *gxp = p.gx + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + 8 * ct);
-            float2 in[3][4];
+            uint8_t *gxp = p.gx + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
+            float2 in[3][NP];
 #pragma unroll
             for (int k = 0; k < 3; ++k)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
+                for (int e = 0; e < NP; ++e)
                     in[k][e] = make_float2(0.f, 0.f);
+            // One row: gradX(i+r) from the window (g0, g1) and the staged
+            // gradY row i+r+2; the three gradWeight taps against x(i+r).
+            auto row = [&](int r) {
+                const Vf<NP> g2 = load_masked<DT, NP>(gys + (size_t)(r + 2) * p.row_bytes, ms[r + 2]);
+                const Vf<NP> xv = unpack<DT, NP>(load_raw<NP>(xs + (size_t)r * p.row_bytes));
+                uint32_t o[NP];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (r < n) {
-                    const V8 g2 = load_masked<DT>(gys + (size_t)(r + 2) * p.row_bytes, ms[r + 2]);
-                    const V8 xv = unpack8<DT>(*reinterpret_cast<const uint4 *>(xs + (size_t)r * p.row_bytes));
-                    uint32_t o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        // gradX: products of two 16-bit values are exact in fp32;
-                        // s + err == p0 + p1 exactly (TwoSum), then one more add
-                        // and the correction: within a hair of the exact sum.
-                        const float2 p0 = mul2(g0.e[e], w2.e[e]);
-                        const float2 p1 = mul2(g1.e[e], w1.e[e]);
-                        const float2 p2 = mul2(g2.e[e], w0.e[e]);
-                        const float2 s = add2(p0, p1);
-                        const float2 bb = sub2(s, p0);
-                        const float2 err = add2(sub2(p0, sub2(s, bb)), sub2(p1, bb));
-                        const float2 t = add2(s, p2);
-                        o[e] = pack2<DT>(add2(t, err));
-                        // gradWeight taps: k = 2 pairs x(i) with gYm(i), k = 1
-                        // with gYm(i+1), k = 0 with gYm(i+2).
-                        in[2][e] = fma2(g0.e[e], xv.e[e], in[2][e]);
-                        in[1][e] = fma2(g1.e[e], xv.e[e], in[1][e]);
-                        in[0][e] = fma2(g2.e[e], xv.e[e], in[0][e]);
-                    }
-                    __stcs(reinterpret_cast<uint4 *>(gxp + (int64_t)r * row_stride),
-                           make_uint4(o[0], o[1], o[2], o[3]));
-                    g0 = g1;
-                    g1 = g2;
+                for (int e = 0; e < NP; ++e) {
+                    // gradX: products of two 16-bit values are exact in fp32;
+                    // s + err == p0 + p1 exactly (TwoSum), then one more add
+                    // and the correction: within a hair of the exact sum.
+                    const float2 p0 = mul2(g0.e[e], w2.e[e]);
+                    const float2 p1 = mul2(g1.e[e], w1.e[e]);
+                    const float2 p2 = mul2(g2.e[e], w0.e[e]);
+                    const float2 s = add2(p0, p1);
+                    const float2 bb = sub2(s, p0);
+                    const float2 err = add2(sub2(p0, sub2(s, bb)), sub2(p1, bb));
+                    const float2 t = add2(s, p2);
+                    o[e] = pack2<DT>(add2(t, err));
+                    // gradWeight taps: k = 2 pairs x(i) with gYm(i), k = 1
+                    // with gYm(i+1), k = 0 with gYm(i+2).
+                    in[2][e] = fma2(g0.e[e], xv.e[e], in[2][e]);
+                    in[1][e] = fma2(g1.e[e], xv.e[e], in[1][e]);
+                    in[0][e] = fma2(g2.e[e], xv.e[e], in[0][e]);
                 }
+                store_cs<NP>(gxp + (int64_t)r * row_stride, o);
+                g0 = g1;
+                g1 = g2;
+            };
+            if (n == R) {
+                // full stage: no per-row predicate, so the loads of all rows
+                // can be issued ahead of the arithmetic
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    row(r);
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (r < n)
+                        row(r);
             }
 #pragma unroll
             for (int k = 0; k < 3; ++k)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
+                for (int e = 0; e < NP; ++e)
                     mid[k][e] = add2(mid[k][e], in[k][e]);
             if (++since_flush == kFlushStages) {
 #pragma unroll
                 for (int k = 0; k < 3; ++k)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        outer[(k * 8 + 2 * e) * nct + ct] += mid[k][e].x;
-                        outer[(k * 8 + 2 * e + 1) * nct + ct] += mid[k][e].y;
+                    for (int e = 0; e < NP; ++e) {
+                        outer[(k * CH + 2 * e) * nct + ct] += mid[k][e].x;
+                        outer[(k * CH + 2 * e + 1) * nct + ct] += mid[k][e].y;
                         mid[k][e] = make_float2(0.f, 0.f);
                     }
                 since_flush = 0;
@@ -511,7 +589,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 }
 
 // ------------------------------------------------------------------ kernels
-template <int DT, int R>
+template <int DT, int R, int NP>
 __global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_constant__ MainParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -537,7 +615,7 @@ __global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_const
     if (threadIdx.x < 32)
         dead = produce<R>(p, smem, r0, r1, lane);
     else
-        dead = consume<DT, R>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
+        dead = consume<DT, R, NP>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
     if (dead && lane == 0)
         atomicOr(&s_err, 1);
     __syncthreads();
@@ -618,21 +696,28 @@ __global__ void __launch_bounds__(kReduceSplits * kReduceLanes) mcc1d_bwd_reduce
 typedef void (*MainFn)(MainParams);
 typedef void (*ReduceFn)(ReduceParams);
 
-template <int DT>
+template <int DT, int NP>
 static MainFn main_for(int R)
 {
     switch (R) {
-    case 4: return mcc1d_bwd_main<DT, 4>;
-    case 6: return mcc1d_bwd_main<DT, 6>;
-    case 8: return mcc1d_bwd_main<DT, 8>;
+    case 4: return mcc1d_bwd_main<DT, 4, NP>;
+    case 6: return mcc1d_bwd_main<DT, 6, NP>;
+    case 8: return mcc1d_bwd_main<DT, 8, NP>;
     default: return nullptr;
     }
+}
+
+static MainFn main_kernel(int dtype, int R, int vec)
+{
+    if (dtype == 0)
+        return vec == 4 ? main_for<0, 2>(R) : main_for<0, 4>(R);
+    return vec == 4 ? main_for<1, 2>(R) : main_for<1, 4>(R);
 }
 
 // cudaFuncSetAttribute once per (kernel, device).
 static bool ensure_smem_attr(const void *fn, int slot_id)
 {
-    static std::atomic<uint64_t> done[8];
+    static std::atomic<uint64_t> done[16];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return false;
@@ -694,11 +779,11 @@ int32_t launch_bwd(const Plan &pl, const void *gradY, const void *x, const void 
     }
 
     const int R = pl.rows_per_stage;
-    MainFn mfn = pl.dtype == 0 ? main_for<0>(R) : main_for<1>(R);
+    MainFn mfn = main_kernel(pl.dtype, R, pl.vec);
     ReduceFn rfn = pl.dtype == 0 ? mcc1d_bwd_reduce<0> : mcc1d_bwd_reduce<1>;
     if (!mfn)
         return kErrCuda;
-    const int attr_slot = pl.dtype * 3 + (R == 4 ? 0 : R == 6 ? 1 : 2);
+    const int attr_slot = (pl.dtype * 2 + (pl.vec == 4 ? 1 : 0)) * 4 + (R == 4 ? 0 : R == 6 ? 1 : 2);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(mfn), attr_slot))
         return kErrCuda;
 

@@ -39,7 +39,13 @@ int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Pla
     // multiple of 64 halves so every staged row is a multiple of 128 bytes.
     p->n_hb = (int32_t)ceil_div(H, kMaxHbWidth);
     p->hb_width = (int32_t)round_up(ceil_div(H, p->n_hb), 64);
-    const int vectors = p->hb_width / 8;
+    // Channels per consumer thread: 8 (16-byte vectors), or 4 when 16-byte
+    // vectors would leave part of the last warp idle and 8-byte vectors fill
+    // whole warps within 4 consumer warps (the case of H-blocks of 384).
+    p->vec = 8;
+    if ((p->hb_width / 8) % 32 != 0 && (p->hb_width / 4) % 32 == 0 && p->hb_width / 4 <= 128)
+        p->vec = 4;
+    const int vectors = p->hb_width / p->vec;
     p->consumer_warps = (int32_t)ceil_div(vectors, 32);
     p->threads = 32 * (p->consumer_warps + 1);
 
@@ -50,7 +56,7 @@ int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Pla
     p->ctas_per_sm = cps;
 
     p->row_bytes = (uint32_t)p->hb_width * 2u;
-    const uint32_t outer_bytes = (uint32_t)p->consumer_warps * 32u * 24u * 4u;
+    const uint32_t outer_bytes = (uint32_t)p->consumer_warps * 32u * 3u * (uint32_t)p->vec * 4u;
     const int64_t budget = kSmemPerSM / cps - kSmemReservedPerCta;
 
     // Rows per stage and ring depth: the deepest R (fewer barrier round trips)

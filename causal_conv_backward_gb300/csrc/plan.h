@@ -46,7 +46,9 @@ struct Plan {
     // H is cut into n_hb blocks of hb_width halves (the last may be narrower).
     int32_t hb_width, n_hb;
     // CTA shape: warp 0 produces (bulk copies), consumer_warps compute; each
-    // consumer thread owns one 16-byte vector (8 halves) of the H-block.
+    // consumer thread owns `vec` consecutive channels (8: a 16-byte vector,
+    // or 4: an 8-byte vector) of the H-block.
+    int32_t vec;
     int32_t consumer_warps, threads;
     int32_t rows_per_stage;  // R: rows of x (and R+2 of gradY) per ring slot
     int32_t stages;          // ring slots
@@ -65,7 +67,7 @@ struct Plan {
     uint32_t slot_bytes;     // (2R + 2) rows
     uint32_t off_mask;       // stages x 32 mask bytes
     uint32_t off_bar;        // 2 x stages mbarriers
-    uint32_t off_outer;      // 24 fp32 accumulators per consumer thread
+    uint32_t off_outer;      // 3 * vec fp32 accumulators per consumer thread
     uint32_t smem_bytes;
     // Workspace layout: header | per-CTA status words | fp32 partials
     // [nslots][W][hb_width].
