@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-mask", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layout", choices=["sbh", "bsh"], default="sbh",
+                    help="bsh: gradY and x live as [B,S,H] buffers seen as [S,B,H] (strided call)")
     ap.add_argument("--graph", action="store_true",
                     help="capture the K timed calls in one CUDA graph (removes host launch gaps)")
     ap.add_argument("--seq-len", type=int, default=0,
@@ -160,9 +162,9 @@ def chosen_workload(args):
     return wl
 
 
-def describe(wl) -> dict:
+def describe(wl, layout="sbh") -> dict:
     mask = "none" if wl.mask[0] == "none" else "(" + ",".join(str(v) for v in wl.mask) + ")"
-    return {"workload": wl.name, "S": wl.S, "B": wl.B, "H": wl.H, "W": wl.W, "io_dtype": wl.dtype,
+    return {"workload": wl.name, "layout": layout, "S": wl.S, "B": wl.B, "H": wl.H, "W": wl.W, "io_dtype": wl.dtype,
             "x_gradY": list(wl.x), "weight": list(wl.w), "mask": mask, "seed": 0,
             "l2": f"inputs {wl.algorithmic_bytes() / 1e9:.1f} GB per step > 129 MB L2; no flush"}
 
@@ -263,6 +265,17 @@ def gpu_arm(args):
     def step(st=None):
         m.mcc1d_bwd(gy, x, w, mask, gx, gw, ws, st or stream, wl.S, wl.B, wl.H, wl.W, code, nbytes)
 
+    if args.layout == "bsh":
+        # the same values held as [B,S,H] buffers and passed as strided views
+        gy_v = gy.transpose(0, 1).contiguous().transpose(0, 1)
+        x_v = x.transpose(0, 1).contiguous().transpose(0, 1)
+        desc = m.tensors(gy_v, x_v, w, mask, gx, gw)
+        nbytes = m.mcc1d_bwd_ex_workspace_size(desc, wl.S, wl.B, wl.H, wl.W, code)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def step(st=None):  # noqa: F811
+            m.mcc1d_bwd_ex(desc, wl.S, wl.B, wl.H, wl.W, code, ws, nbytes, st or stream)
+
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
@@ -309,7 +322,7 @@ def gpu_arm(args):
 
     # end to end: pinned host inputs -> device -> call -> host outputs, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.layout == "sbh":
         hx = {k: v for k, v in host.items() if v is not None}
         out_gx = torch.empty(gx.shape, dtype=torch.int16, pin_memory=True)
         out_gw = torch.empty(gw.shape, dtype=torch.int16, pin_memory=True)
@@ -367,7 +380,7 @@ def gpu_arm(args):
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(t_max / K * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded generator; fp16 bit patterns)",
-            "config": describe(wl), "tokens_h_per_s": float(f"{tokens_h:.4e}"),
+            "config": describe(wl, args.layout), "tokens_h_per_s": float(f"{tokens_h:.4e}"),
             "frac_of_peak": round(value / world / peak, 4),
             "e2e": e2e, "gpu_launches": 2 * K, "roofline": roofline, "cpu_baseline": cpu,
             "timing": "one CUDA graph of K calls" if graph is not None else "K direct C-ABI calls",

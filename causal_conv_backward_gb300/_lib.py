@@ -22,6 +22,16 @@ _lock = threading.Lock()
 _lib = None
 
 
+class Mcc1dTensors(ctypes.Structure):
+    """Mirror of ``mcc1d_tensors``: pointers plus strides (elements; the
+    mask's in bytes), outermost dimension first."""
+    _fields_ = [("gradY", ctypes.c_void_p), ("gradY_strides", ctypes.c_int64 * 3),
+                ("x", ctypes.c_void_p), ("x_strides", ctypes.c_int64 * 3),
+                ("weight", ctypes.c_void_p), ("weight_strides", ctypes.c_int64 * 2),
+                ("mask", ctypes.c_void_p), ("mask_strides", ctypes.c_int64 * 2),
+                ("gradX", ctypes.c_void_p), ("gradWeight", ctypes.c_void_p)]
+
+
 class Mcc1dError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
@@ -48,6 +58,11 @@ def load():
         lib.mcc1d_bwd_workspace_size.restype = i32
         lib.mcc1d_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, u64]
         lib.mcc1d_bwd.restype = i32
+        lib.mcc1d_bwd_ex_workspace_size.argtypes = [ctypes.POINTER(Mcc1dTensors), i64, i64, i64, i64,
+                                                    i32, ctypes.POINTER(u64)]
+        lib.mcc1d_bwd_ex_workspace_size.restype = i32
+        lib.mcc1d_bwd_ex.argtypes = [ctypes.POINTER(Mcc1dTensors), i64, i64, i64, i64, i32, vp, u64, vp]
+        lib.mcc1d_bwd_ex.restype = i32
         lib.mcc1d_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32]
         lib.mcc1d_bwd_noalloc.restype = i32
         lib.mcc1d_bwd_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
@@ -97,6 +112,39 @@ def mcc1d_bwd(gradY, x, weight, mask_or_null, gradX, gradWeight, workspace, stre
         raise Mcc1dError(st, "mcc1d_bwd")
 
 
+def tensors(gradY, x, weight, mask, gradX, gradWeight) -> Mcc1dTensors:
+    """Descriptor of torch tensors (their data pointers and element strides)."""
+    t = Mcc1dTensors()
+    t.gradY, t.x, t.weight = gradY.data_ptr(), x.data_ptr(), weight.data_ptr()
+    t.gradY_strides[:] = list(gradY.stride())
+    t.x_strides[:] = list(x.stride())
+    t.weight_strides[:] = list(weight.stride())
+    if mask is not None:
+        t.mask = mask.data_ptr()
+        t.mask_strides[:] = [st * mask.element_size() for st in mask.stride()]
+    t.gradX, t.gradWeight = gradX.data_ptr(), gradWeight.data_ptr()
+    return t
+
+
+def mcc1d_bwd_ex_workspace_size(t: Mcc1dTensors, S, B, H, W, dtype) -> int:
+    out = ctypes.c_uint64(0)
+    st = load().mcc1d_bwd_ex_workspace_size(ctypes.byref(t), S, B, H, W, dtype_code(dtype),
+                                            ctypes.byref(out))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_bwd_ex_workspace_size")
+    return int(out.value)
+
+
+def mcc1d_bwd_ex(t: Mcc1dTensors, S, B, H, W, dtype, workspace, workspace_bytes, stream) -> None:
+    """Enqueue the backward on strided tensors described by ``t``."""
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = load().mcc1d_bwd_ex(ctypes.byref(t), S, B, H, W, dtype_code(dtype), _ptr(workspace),
+                             int(workspace_bytes), stream or None)
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_bwd_ex")
+
+
 def mcc1d_bwd_noalloc(gradY, x, weight, mask_or_null, gradX, gradWeight, stream,
                       S, B, H, W, dtype) -> None:
     """Enqueue the backward with the library's fixed scratch array instead of a
@@ -134,30 +182,36 @@ def mcc1d_version() -> int:
 def backward(gradY, x, weight, mask=None, *, gradX=None, gradWeight=None, workspace=None,
              stream=None):
     """Convenience call on torch CUDA tensors: gradY, x [S,B,H], weight [3,H]
-    (bf16 or fp16), mask [B,S] bool/uint8 or None. Allocates whatever output
-    or workspace is not given (with torch) and returns (gradX, gradWeight)."""
+    (bf16 or fp16), mask [B,S] bool/uint8 or None; inputs may be strided
+    views. Allocates whatever output or workspace is not given (with torch)
+    and returns (gradX, gradWeight)."""
     import torch
 
     S, B, H = gradY.shape
     W = weight.shape[0]
     code = dtype_code(gradY.dtype)
     for t in (gradY, x, weight):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("gradY, x and weight must be contiguous CUDA tensors")
-    if mask is not None:
-        if mask.dtype == torch.bool:
-            mask = mask.view(torch.uint8)
-        if not mask.is_contiguous():
-            raise ValueError("mask must be contiguous")
+        if not t.is_cuda:
+            raise ValueError("gradY, x and weight must be CUDA tensors")
+    if mask is not None and mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
     if gradX is None:
-        gradX = torch.empty_like(gradY)
+        gradX = torch.empty((S, B, H), dtype=gradY.dtype, device=gradY.device)
     if gradWeight is None:
-        gradWeight = torch.empty_like(weight)
-    nbytes = mcc1d_bwd_workspace_size(S, B, H, W, code, mask is not None)
-    if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=gradY.device)
+        gradWeight = torch.empty((W, H), dtype=weight.dtype, device=weight.device)
     if stream is None:
         stream = torch.cuda.current_stream(gradY.device)
-    mcc1d_bwd(gradY, x, weight, mask, gradX, gradWeight, workspace, stream, S, B, H, W, code,
-              workspace.numel() * workspace.element_size())
+    dense = all(t.is_contiguous() for t in (gradY, x, weight)) and (mask is None or mask.is_contiguous())
+    if dense:
+        nbytes = mcc1d_bwd_workspace_size(S, B, H, W, code, mask is not None)
+    else:
+        desc = tensors(gradY, x, weight, mask, gradX, gradWeight)
+        nbytes = mcc1d_bwd_ex_workspace_size(desc, S, B, H, W, code)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=gradY.device)
+    wsb = workspace.numel() * workspace.element_size()
+    if dense:
+        mcc1d_bwd(gradY, x, weight, mask, gradX, gradWeight, workspace, stream, S, B, H, W, code, wsb)
+    else:
+        mcc1d_bwd_ex(desc, S, B, H, W, code, workspace, wsb, stream)
     return gradX, gradWeight

@@ -43,8 +43,124 @@ extern "C" int32_t mcc1d_bwd(const void *gradY, const void *x, const void *weigh
         return kErrInvalid;
     if (workspace_bytes < p.ws_bytes)
         return kErrWorkspace;
-    return launch_bwd(p, gradY, x, weight, mask_or_null, gradX, gradWeight, workspace,
-                      static_cast<cudaStream_t>(stream));
+    return launch_bwd(p, dense_layout(S, B, H), gradY, x, weight, mask_or_null, gradX, gradWeight,
+                      workspace, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+// Plan of a strided call: which inputs are gathered into the workspace first,
+// and where.
+struct ExPlan {
+    Plan plan;
+    Layout L;          // layout the main kernel reads (dense for gathered inputs)
+    Layout in;         // the caller's layout
+    bool pack_gy, pack_x;
+    uint64_t off_gy, off_x, bytes;
+};
+
+uint64_t round256(uint64_t v) { return (v + 255u) & ~(uint64_t)255u; }
+
+// A 16-bit [S,B,H] input is streamed in place when its rows are contiguous
+// along H and start on 16-byte boundaries.
+bool streamable(const void *p, const int64_t st[3])
+{
+    return st[2] == 1 && ((uintptr_t)p & 15u) == 0 && (st[0] * 2) % 16 == 0 && (st[1] * 2) % 16 == 0;
+}
+
+int32_t make_ex(const mcc1d_tensors *t, int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                ExPlan *e)
+{
+    if (!t || !t->gradY || !t->x || !t->weight || !t->gradX || !t->gradWeight)
+        return kErrNull;
+    const int32_t st = make_plan(S, B, H, W, dtype, &e->plan);
+    if (st != kOk)
+        return st;
+    Layout in;
+    const int64_t dims3[3] = {S, B, H};
+    for (int d = 0; d < 3; ++d) {
+        in.gy[d] = dims3[d] == 1 ? 0 : t->gradY_strides[d];
+        in.x[d] = dims3[d] == 1 ? 0 : t->x_strides[d];
+        if (t->gradY_strides[d] < 0 || t->x_strides[d] < 0)
+            return kErrInvalid;
+    }
+    const int64_t dimsw[2] = {W, H}, dimsm[2] = {B, S};
+    for (int d = 0; d < 2; ++d) {
+        in.w[d] = dimsw[d] == 1 ? 0 : t->weight_strides[d];
+        in.m[d] = dimsm[d] == 1 ? 0 : t->mask_strides[d];
+        if (t->weight_strides[d] < 0 || (t->mask && t->mask_strides[d] < 0))
+            return kErrInvalid;
+    }
+    if (((uintptr_t)t->gradY & 1u) || ((uintptr_t)t->x & 1u) || ((uintptr_t)t->weight & 1u) ||
+        ((uintptr_t)t->gradX & 15u) || ((uintptr_t)t->gradWeight & 15u))
+        return kErrInvalid;
+    e->in = in;
+    e->L = in;
+    const uint64_t tensor_bytes = (uint64_t)S * (uint64_t)B * (uint64_t)H * 2u;
+    e->pack_gy = !streamable(t->gradY, in.gy);
+    e->pack_x = !streamable(t->x, in.x);
+    const Layout dense = dense_layout(S, B, H);
+    uint64_t off = round256(e->plan.ws_bytes);
+    e->off_gy = e->off_x = 0;
+    if (e->pack_gy) {
+        e->off_gy = off;
+        off = round256(off + tensor_bytes);
+        for (int d = 0; d < 3; ++d)
+            e->L.gy[d] = dense.gy[d];
+    }
+    if (e->pack_x) {
+        e->off_x = off;
+        off = round256(off + tensor_bytes);
+        for (int d = 0; d < 3; ++d)
+            e->L.x[d] = dense.x[d];
+    }
+    e->bytes = off;
+    return kOk;
+}
+
+}  // namespace
+
+extern "C" int32_t mcc1d_bwd_ex_workspace_size(const mcc1d_tensors *t, int64_t S, int64_t B,
+                                               int64_t H, int64_t W, int32_t dtype,
+                                               uint64_t *bytes_out)
+{
+    if (!bytes_out)
+        return kErrNull;
+    ExPlan e;
+    const int32_t st = make_ex(t, S, B, H, W, dtype, &e);
+    if (st != kOk)
+        return st;
+    *bytes_out = e.bytes;
+    return kOk;
+}
+
+extern "C" int32_t mcc1d_bwd_ex(const mcc1d_tensors *t, int64_t S, int64_t B, int64_t H, int64_t W,
+                                int32_t dtype, void *workspace, uint64_t workspace_bytes, void *stream)
+{
+    ExPlan e;
+    const int32_t st = make_ex(t, S, B, H, W, dtype, &e);
+    if (st != kOk)
+        return st;
+    if (!workspace)
+        return kErrNull;
+    if (!aligned16(workspace))
+        return kErrInvalid;
+    if (workspace_bytes < e.bytes)
+        return kErrWorkspace;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const void *gy = t->gradY, *x = t->x;
+    if (e.pack_gy) {
+        if (launch_pack(t->gradY, e.in.gy, ws + e.off_gy, S, B, H, s) != kOk)
+            return kErrCuda;
+        gy = ws + e.off_gy;
+    }
+    if (e.pack_x) {
+        if (launch_pack(t->x, e.in.x, ws + e.off_x, S, B, H, s) != kOk)
+            return kErrCuda;
+        x = ws + e.off_x;
+    }
+    return launch_bwd(e.plan, e.L, gy, x, t->weight, t->mask, t->gradX, t->gradWeight, workspace, s);
 }
 
 extern "C" int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *status_out)

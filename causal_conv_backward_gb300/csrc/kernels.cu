@@ -60,6 +60,10 @@ struct MainParams {
     int32_t B, hb_width, ncta, stages;
     uint32_t row_bytes, slot_bytes, off_mask, off_bar, off_outer;
     int32_t c_lo[kMaxHb], slot_base[kMaxHb];
+    // Input strides (elements; mask bytes). gradY and x have unit H stride.
+    int64_t gy_s, gy_b, x_s, x_b, w_k, w_h, m_b, m_s;
+    int32_t contig_rows;   // a stage's rows are adjacent in memory (one copy per tensor)
+    int32_t w_vec;         // weight rows can be read as aligned vectors
 };
 
 struct ReduceParams {
@@ -323,7 +327,7 @@ __device__ __forceinline__ uint32_t stage_mask_byte(const MainParams &p, const C
         return 0;  // past the end of the sequence: zero padding
     if (p.mask == nullptr)
         return 1;
-    return __ldg(p.mask + (int64_t)c.j * p.S + row) != 0 ? 1u : 0u;
+    return __ldg(p.mask + (int64_t)c.j * p.m_b + row * p.m_s) != 0 ? 1u : 0u;
 }
 
 template <int R>
@@ -333,8 +337,7 @@ __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
     const uint32_t ring0 = smem_u32(smem);
-    const int64_t row_elems = (int64_t)p.B * p.H;  // elements between rows i and i+1
-    const bool contiguous = p.B == 1 && p.H == p.hb_width;
+    const bool contiguous = p.contig_rows != 0;
 
     Cursor cur;
     cur.init(r0, r1, p.S, p.BS);
@@ -374,22 +377,23 @@ __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
         __syncwarp();
         const uint32_t slot_base = ring0 + (uint32_t)slot * p.slot_bytes;
         if (contiguous) {
-            // B = 1 and one H-block: the stage's rows are adjacent both in
-            // memory and in the slot, so one copy per tensor moves them.
+            // B = 1, one H-block and rows packed back to back: the stage's rows
+            // are adjacent both in memory and in the slot, so one copy per
+            // tensor moves them.
             if (lane == 0) {
                 if (nG > 0)
-                    bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.gy + 2 * (cur.i + q0) * p.H,
+                    bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.gy + 2 * (cur.i + q0) * p.gy_s,
                              (uint32_t)nG * wbytes, bar_full0 + 8u * slot);
-                bulk_g2s(slot_base + (uint32_t)(R + 2) * p.row_bytes, p.x + 2 * cur.i * p.H,
+                bulk_g2s(slot_base + (uint32_t)(R + 2) * p.row_bytes, p.x + 2 * cur.i * p.x_s,
                          (uint32_t)n * wbytes, bar_full0 + 8u * slot);
             }
         } else if (lane < nG) {
             const int q = q0 + lane;
-            const int64_t e = ((cur.i + q) * p.B + cur.j) * p.H + hb0;
+            const int64_t e = (cur.i + q) * p.gy_s + (int64_t)cur.j * p.gy_b + hb0;
             bulk_g2s(slot_base + (uint32_t)q * p.row_bytes, p.gy + 2 * e, wbytes, bar_full0 + 8u * slot);
         } else if (lane < nG + n) {
             const int q = lane - nG;
-            const int64_t e = (cur.i + q) * row_elems + (int64_t)cur.j * p.H + hb0;
+            const int64_t e = (cur.i + q) * p.x_s + (int64_t)cur.j * p.x_b + hb0;
             bulk_g2s(slot_base + (uint32_t)(R + 2 + q) * p.row_bytes, p.x + 2 * e, wbytes,
                      bar_full0 + 8u * slot);
         }
@@ -412,6 +416,23 @@ __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 }
 
 // ------------------------------------------------------------------ consumers
+// Weight taps k for channels h .. h + 2*NP - 1: one vector load when the
+// weight rows are dense and aligned, else one 16-bit load per channel.
+template <int DT, int NP>
+__device__ __forceinline__ Vf<NP> load_weight(const MainParams &p, int k, int64_t h)
+{
+    if (p.w_vec)
+        return unpack<DT, NP>(ldg_raw<NP>(p.w + k * p.w_k + h));
+    Raw<NP> r;
+#pragma unroll
+    for (int e = 0; e < NP; ++e) {
+        const uint32_t lo = __ldg(p.w + k * p.w_k + (h + 2 * e) * p.w_h);
+        const uint32_t hi = __ldg(p.w + k * p.w_k + (h + 2 * e + 1) * p.w_h);
+        r.u[e] = lo | (hi << 16);
+    }
+    return unpack<DT, NP>(r);
+}
+
 template <int DT, int R, int NP>
 __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t r1, int ct, int lane)
 {
@@ -489,9 +510,9 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
             const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
             active = CH * ct < width;
             if (active) {
-                w0 = unpack<DT, NP>(ldg_raw<NP>(p.w + 0 * p.H + hb0 + CH * ct));
-                w1 = unpack<DT, NP>(ldg_raw<NP>(p.w + 1 * p.H + hb0 + CH * ct));
-                w2 = unpack<DT, NP>(ldg_raw<NP>(p.w + 2 * p.H + hb0 + CH * ct));
+                w0 = load_weight<DT, NP>(p, 0, hb0 + CH * ct);
+                w1 = load_weight<DT, NP>(p, 1, hb0 + CH * ct);
+                w2 = load_weight<DT, NP>(p, 2, hb0 + CH * ct);
             }
         }
         if (!dead) {
@@ -692,6 +713,27 @@ __global__ void __launch_bounds__(kReduceSplits * kReduceLanes) mcc1d_bwd_reduce
     }
 }
 
+// Gather of a strided [S,B,H] 16-bit tensor into dense rows, 8 channels
+// (one 16-byte store) per thread and step.
+__global__ void __launch_bounds__(256) mcc1d_pack(const uint16_t *src, int64_t s_s, int64_t s_b,
+                                                  int64_t s_h, uint16_t *dst, int64_t S, int64_t B,
+                                                  int64_t H)
+{
+    const int64_t per_row = H / 8;
+    const int64_t groups = S * B * per_row;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t hv = g % per_row, row = g / per_row;
+        const int64_t j = row % B, i = row / B;
+        const uint16_t *sp = src + i * s_s + j * s_b + hv * 8 * s_h;
+        uint32_t u[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            u[e] = (uint32_t)__ldg(sp + 2 * e * s_h) | ((uint32_t)__ldg(sp + (2 * e + 1) * s_h) << 16);
+        *reinterpret_cast<uint4 *>(dst + row * H + hv * 8) = make_uint4(u[0], u[1], u[2], u[3]);
+    }
+}
+
 // ------------------------------------------------------------------ host launch
 typedef void (*MainFn)(MainParams);
 typedef void (*ReduceFn)(ReduceParams);
@@ -732,9 +774,22 @@ static bool ensure_smem_attr(const void *fn, int slot_id)
     return true;
 }
 
-int32_t launch_bwd(const Plan &pl, const void *gradY, const void *x, const void *weight,
-                   const uint8_t *mask, void *gradX, void *gradWeight, void *workspace,
-                   cudaStream_t stream)
+int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_t S, int64_t B,
+                    int64_t H, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(kNumSMs * 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    if (cudaLaunchKernelEx(&cfg, mcc1d_pack, static_cast<const uint16_t *>(src), strides[0], strides[1],
+                           strides[2], static_cast<uint16_t *>(dst), S, B, H) != cudaSuccess)
+        return kErrCuda;
+    return kOk;
+}
+
+int32_t launch_bwd(const Plan &pl, const Layout &L, const void *gradY, const void *x,
+                   const void *weight, const uint8_t *mask, void *gradX, void *gradWeight,
+                   void *workspace, cudaStream_t stream)
 {
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     MainParams mp;
@@ -762,6 +817,16 @@ int32_t launch_bwd(const Plan &pl, const void *gradY, const void *x, const void 
         mp.c_lo[h] = pl.c_lo[h];
         mp.slot_base[h] = pl.slot_base[h];
     }
+    mp.gy_s = L.gy[0];
+    mp.gy_b = L.gy[1];
+    mp.x_s = L.x[0];
+    mp.x_b = L.x[1];
+    mp.w_k = L.w[0];
+    mp.w_h = L.w[1];
+    mp.m_b = L.m[0];
+    mp.m_s = L.m[1];
+    mp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && L.gy[0] == pl.H && L.x[0] == pl.H) ? 1 : 0;
+    mp.w_vec = (L.w[1] == 1 && (L.w[0] * 2) % 16 == 0 && ((uintptr_t)weight & 15u) == 0) ? 1 : 0;
 
     ReduceParams rp;
     rp.part = mp.part;

@@ -8,10 +8,17 @@
 
 namespace mcc1d {
 
-// Enqueues the main and reduce kernels of plan `p` on `stream`. Pointers have
-// been validated by the caller. Returns kOk or kErrCuda.
-int32_t launch_bwd(const Plan &p, const void *gradY, const void *x, const void *weight,
-                   const uint8_t *mask, void *gradX, void *gradWeight, void *workspace,
-                   cudaStream_t stream);
+// Enqueues the main and reduce kernels of plan `p` on `stream`. gradY and x
+// must be row-streamable under `L` (unit H stride, 16-byte aligned rows);
+// weight and mask may have any strides. Pointers have been validated by the
+// caller. Returns kOk or kErrCuda.
+int32_t launch_bwd(const Plan &p, const Layout &L, const void *gradY, const void *x,
+                   const void *weight, const uint8_t *mask, void *gradX, void *gradWeight,
+                   void *workspace, cudaStream_t stream);
+
+// Enqueues a gather of a strided 16-bit [S,B,H] tensor into a dense one
+// (dst 16-byte aligned). Returns kOk or kErrCuda.
+int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_t S, int64_t B,
+                    int64_t H, cudaStream_t stream);
 
 }  // namespace mcc1d

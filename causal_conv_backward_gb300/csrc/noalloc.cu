@@ -72,6 +72,6 @@ extern "C" int32_t mcc1d_bwd_noalloc(const void *gradY, const void *x, const voi
         return sa;
     // Nothing in the scratch has to start at zero: each call writes every
     // status word and partial it later reads.
-    return launch_bwd(p, gradY, x, weight, mask_or_null, gradX, gradWeight, scratch,
-                      static_cast<cudaStream_t>(stream));
+    return launch_bwd(p, dense_layout(S, B, H), gradY, x, weight, mask_or_null, gradX, gradWeight,
+                      scratch, static_cast<cudaStream_t>(stream));
 }

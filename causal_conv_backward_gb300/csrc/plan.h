@@ -76,6 +76,26 @@ struct Plan {
     int32_t reduce_blocks;
 };
 
+// Strides of the inputs in elements (the mask's in bytes), outermost first:
+// gradY and x [S,B,H], weight [W,H], mask [B,S]. The dense layout is
+// gradY/x (B*H, H, 1), weight (H, 1), mask (S, 1).
+struct Layout {
+    int64_t gy[3], x[3], w[2], m[2];
+};
+
+inline Layout dense_layout(int64_t S, int64_t B, int64_t H)
+{
+    Layout L;
+    L.gy[0] = L.x[0] = B * H;
+    L.gy[1] = L.x[1] = H;
+    L.gy[2] = L.x[2] = 1;
+    L.w[0] = H;
+    L.w[1] = 1;
+    L.m[0] = S;
+    L.m[1] = 1;
+    return L;
+}
+
 // Shape and dtype checks of the page's constraints. Returns kOk, kErrInvalid
 // (dtype) or kErrShape.
 int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype);

@@ -125,6 +125,59 @@ int32_t mcc1d_bwd(const void *gradY, const void *x, const void *weight,
                   uint64_t workspace_bytes);
 
 /*
+ * Tensors of one call with explicit strides: the page's inputs may be
+ * non-contiguous (the 非连续Tensor column of its parameter table), its
+ * outputs may not. Strides count ELEMENTS for the 16-bit tensors and BYTES for
+ * the mask, outermost dimension first; no stride may be negative (a zero
+ * stride repeats data). Strides of dimensions of size 1 are ignored.
+ *
+ *   gradY, x      [S,B,H] inputs: strides {S, B, H}
+ *   weight        [W,H]   input:  strides {W, H}
+ *   mask          [B,S]   input bytes or NULL: strides {B, S}
+ *   gradX         [S,B,H] output, dense (strides {B*H, H, 1})
+ *   gradWeight    [W,H]   output, dense (strides {H, 1})
+ *
+ * gradY and x with unit H stride and 16-byte aligned rows (base pointer and
+ * the S and B strides in bytes multiples of 16, e.g. a [B,S,H] buffer seen
+ * as [S,B,H], or an H-slice of a wider tensor) are streamed in place. Any
+ * other layout of gradY or x is first gathered into a dense copy inside the
+ * workspace, which then includes S*B*H*2 bytes per such tensor. weight and
+ * mask are read in place with any strides.
+ */
+typedef struct mcc1d_tensors {
+    const void *gradY;
+    int64_t gradY_strides[3];
+    const void *x;
+    int64_t x_strides[3];
+    const void *weight;
+    int64_t weight_strides[2];
+    const uint8_t *mask;
+    int64_t mask_strides[2];
+    void *gradX;
+    void *gradWeight;
+} mcc1d_tensors;
+
+/*
+ * Phase 1 for strided tensors (page: the same GetWorkspaceSize call, which
+ * receives the tensors themselves). The workspace size depends on the
+ * layouts and base pointers of gradY and x. Validation as
+ * mcc1d_bwd_workspace_size, plus: MCC1D_ERR_PARAM_NULLPTR for a null
+ * descriptor or required pointer; MCC1D_ERR_PARAM_INVALID for a negative
+ * stride, a 16-bit input pointer that is not 2-byte aligned, or an output
+ * pointer that is not 16-byte aligned.
+ */
+int32_t mcc1d_bwd_ex_workspace_size(const mcc1d_tensors *t, int64_t S, int64_t B, int64_t H,
+                                    int64_t W, int32_t dtype, uint64_t *bytes_out);
+
+/*
+ * Phase 2 for strided tensors: as mcc1d_bwd, with the tensors described by
+ * `t`. Results are bitwise identical to mcc1d_bwd on dense copies of the same
+ * values. Errors as mcc1d_bwd_ex_workspace_size and mcc1d_bwd.
+ */
+int32_t mcc1d_bwd_ex(const mcc1d_tensors *t, int64_t S, int64_t B, int64_t H, int64_t W,
+                     int32_t dtype, void *workspace, uint64_t workspace_bytes, void *stream);
+
+/*
  * Device-side status of the last mcc1d_bwd that used `workspace`: waits for
  * `stream` to finish, then copies the status word that the call left in the
  * workspace to *status_out (MCC1D_OK, or MCC1D_ERR_DEVICE_TIMEOUT when a

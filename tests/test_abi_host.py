@@ -105,3 +105,61 @@ def test_status_strings(lib):
         assert s.startswith("MCC1D_")
     assert m.mcc1d_status_string(42) == "unknown mcc1d status"
     assert m.mcc1d_version() >= 100
+
+
+# ------------------------------------------------------------- strided calls
+def desc(gy=0x10000, x=0x20000, w=0x30000, mask=None, gx=0x40000, gw=0x50000,
+         gys=None, xs=None, ws_=None, ms=None, S=64, B=2, H=384):
+    t = m.Mcc1dTensors()
+    t.gradY, t.x, t.weight, t.mask, t.gradX, t.gradWeight = gy, x, w, mask, gx, gw
+    t.gradY_strides[:] = gys or [B * H, H, 1]
+    t.x_strides[:] = xs or [B * H, H, 1]
+    t.weight_strides[:] = ws_ or [H, 1]
+    t.mask_strides[:] = ms or [S, 1]
+    return t
+
+
+def ex_size(t, S=64, B=2, H=384, W=3, dt=0):
+    v = ctypes.c_uint64(7)
+    st = m.load().mcc1d_bwd_ex_workspace_size(ctypes.byref(t), S, B, H, W, dt, ctypes.byref(v))
+    return st, v.value
+
+
+def test_ex_workspace_dense_needs_no_copies(lib):
+    st, n = ex_size(desc())
+    base = ws(64, 2, 384)[1]
+    assert st == 0 and base <= n < base + 256
+
+
+def test_ex_workspace_counts_gathered_inputs(lib):
+    S, B, H = 64, 2, 384
+    E2 = S * B * H * 2
+    base = ex_size(desc())[1]
+    # a [B,S,H] buffer seen as [S,B,H] streams in place
+    assert ex_size(desc(gys=[H, S * H, 1], xs=[H, S * H, 1]))[1] == base
+    # H stride 2, or a base pointer off a 16-byte boundary, is gathered first
+    assert ex_size(desc(gys=[2 * B * H, 2 * H, 2]))[1] == base + E2
+    assert ex_size(desc(x=0x20002))[1] == base + E2
+    assert ex_size(desc(gys=[B * H, H, 2], x=0x20002))[1] == base + 2 * E2
+    # odd row strides break 16-byte row alignment
+    assert ex_size(desc(xs=[B * H + 1, H, 1]))[1] == base + E2
+    # weight and mask strides never cost workspace
+    assert ex_size(desc(ws_=[1, 3], mask=0x60001, ms=[1, 2]))[1] == base
+
+
+def test_ex_rejects(lib):
+    assert m.load().mcc1d_bwd_ex_workspace_size(None, 64, 2, 384, 3, 0, ctypes.byref(ctypes.c_uint64())) == NULLPTR
+    assert ex_size(desc(gy=None))[0] == NULLPTR
+    assert ex_size(desc(gys=[-1, 384, 1]))[0] == INVALID
+    assert ex_size(desc(ws_=[384, -1]))[0] == INVALID
+    assert ex_size(desc(mask=0x60000, ms=[-64, 1]))[0] == INVALID
+    assert ex_size(desc(gy=0x10001))[0] == INVALID        # not 2-byte aligned
+    assert ex_size(desc(gx=0x40008))[0] == INVALID        # outputs stay 16-byte aligned
+    assert ex_size(desc(), B=33)[0] == SHAPE
+    assert ex_size(desc(), dt=3)[0] == INVALID
+    t = desc()
+    need = ex_size(t)[1]
+    call = m.load().mcc1d_bwd_ex
+    assert call(ctypes.byref(t), 64, 2, 384, 3, 0, None, need, None) == NULLPTR
+    assert call(ctypes.byref(t), 64, 2, 384, 3, 0, 0x70008, need, None) == INVALID
+    assert call(ctypes.byref(t), 64, 2, 384, 3, 0, 0x70000, need - 1, None) == WORKSPACE
