@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-mask", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["bwd", "fwd"], default="bwd",
+                    help="fwd: time the forward kernel (mcc1d_fwd) on the same workload")
     ap.add_argument("--layout", choices=["sbh", "bsh"], default="sbh",
                     help="bsh: gradY and x live as [B,S,H] buffers seen as [S,B,H] (strided call)")
     ap.add_argument("--graph", action="store_true",
@@ -265,6 +267,12 @@ def gpu_arm(args):
     def step(st=None):
         m.mcc1d_bwd(gy, x, w, mask, gx, gw, ws, st or stream, wl.S, wl.B, wl.H, wl.W, code, nbytes)
 
+    if args.op == "fwd":
+        y = torch.empty_like(x)
+
+        def step(st=None):  # noqa: F811
+            m.mcc1d_fwd(x, w, mask, y, st or stream, wl.S, wl.B, wl.H, wl.W, code)
+
     if args.layout == "bsh":
         # the same values held as [B,S,H] buffers and passed as strided views
         gy_v = gy.transpose(0, 1).contiguous().transpose(0, 1)
@@ -279,7 +287,7 @@ def gpu_arm(args):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
-    if m.mcc1d_bwd_device_status(ws, stream) != 0:
+    if args.op == "bwd" and m.mcc1d_bwd_device_status(ws, stream) != 0:
         raise SystemExit("bench.py: device-side status is not OK")
 
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
@@ -315,14 +323,14 @@ def gpu_arm(args):
     elapsed = start.elapsed_time(end) / 1e3
     per_call = ([elapsed / K] * K if graph is not None
                 else [a.elapsed_time(b) / 1e3 for a, b in ev])
-    alg = wl.algorithmic_bytes()
+    alg = wl.algorithmic_bytes() if args.op == "bwd" else wl.fwd_algorithmic_bytes()
     t_max, bytes_all = aggregate(dist, elapsed, float(alg) * K, dev)
     value = bytes_all / t_max / 1e9
     tokens_h = float(wl.E) * K * world / t_max
 
     # end to end: pinned host inputs -> device -> call -> host outputs, every step
     e2e = None
-    if not args.no_e2e and args.layout == "sbh":
+    if not args.no_e2e and args.layout == "sbh" and args.op == "bwd":
         hx = {k: v for k, v in host.items() if v is not None}
         out_gx = torch.empty(gx.shape, dtype=torch.int16, pin_memory=True)
         out_gw = torch.empty(gw.shape, dtype=torch.int16, pin_memory=True)
@@ -362,12 +370,13 @@ def gpu_arm(args):
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
-                "kernel": "mcc1d_bwd_main (timed as the whole call: main + reduce)",
+                "kernel": ("mcc1d_bwd_main (timed as the whole call: main + reduce)" if args.op == "bwd"
+                           else "mcc1d_fwd_main"),
                 "algorithmic_bytes_per_launch": alg,
                 "median_call_ms": round(statistics.median(per_call) * 1e3, 4)}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.op == "bwd":
         t, sample, nt = time_oracle(wl, CPU_SAMPLE_S, steps=1, warmup=0)
         cpu = {"value": round(sample.algorithmic_bytes() / t / 1e9, 4), "unit": "GB/s",
                "cores": nt, "kind": "oracle",
@@ -382,7 +391,9 @@ def gpu_arm(args):
             "data": "synthetic (seeded generator; fp16 bit patterns)",
             "config": describe(wl, args.layout), "tokens_h_per_s": float(f"{tokens_h:.4e}"),
             "frac_of_peak": round(value / world / peak, 4),
-            "e2e": e2e, "gpu_launches": 2 * K, "roofline": roofline, "cpu_baseline": cpu,
+            "op": args.op,
+            "e2e": e2e, "gpu_launches": (2 if args.op == "bwd" else 1) * K, "roofline": roofline,
+            "cpu_baseline": cpu,
             "timing": "one CUDA graph of K calls" if graph is not None else "K direct C-ABI calls",
             "clocks": clocks,
         }

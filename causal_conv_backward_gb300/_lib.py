@@ -63,6 +63,8 @@ def load():
         lib.mcc1d_bwd_ex_workspace_size.restype = i32
         lib.mcc1d_bwd_ex.argtypes = [ctypes.POINTER(Mcc1dTensors), i64, i64, i64, i64, i32, vp, u64, vp]
         lib.mcc1d_bwd_ex.restype = i32
+        lib.mcc1d_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, vp]
+        lib.mcc1d_fwd.restype = i32
         lib.mcc1d_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32]
         lib.mcc1d_bwd_noalloc.restype = i32
         lib.mcc1d_bwd_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
@@ -143,6 +145,30 @@ def mcc1d_bwd_ex(t: Mcc1dTensors, S, B, H, W, dtype, workspace, workspace_bytes,
                              int(workspace_bytes), stream or None)
     if st != 0:
         raise Mcc1dError(st, "mcc1d_bwd_ex")
+
+
+def mcc1d_fwd(x, weight, mask_or_null, y, stream, S, B, H, W, dtype, device_status=None) -> None:
+    """Enqueue the forward y = mask * causal depthwise conv(x, weight)."""
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = load().mcc1d_fwd(_ptr(x), _ptr(weight), _ptr(mask_or_null), _ptr(y), stream or None,
+                          S, B, H, W, dtype_code(dtype), _ptr(device_status))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_fwd")
+
+
+def forward(x, weight, mask=None, *, y=None, stream=None):
+    """Convenience forward on dense torch CUDA tensors; returns y."""
+    import torch
+    S, B, H = x.shape
+    if mask is not None and mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    if y is None:
+        y = torch.empty_like(x)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    mcc1d_fwd(x, weight, mask, y, stream, S, B, H, weight.shape[0], dtype_code(x.dtype))
+    return y
 
 
 def mcc1d_bwd_noalloc(gradY, x, weight, mask_or_null, gradX, gradWeight, stream,

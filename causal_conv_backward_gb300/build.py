@@ -37,7 +37,7 @@ def sources() -> list[str]:
 def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
-    deps = sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    deps = sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     t = os.path.getmtime(LIB)
     return any(os.path.getmtime(d) > t for d in deps)
 

@@ -163,6 +163,22 @@ extern "C" int32_t mcc1d_bwd_ex(const mcc1d_tensors *t, int64_t S, int64_t B, in
     return launch_bwd(e.plan, e.L, gy, x, t->weight, t->mask, t->gradX, t->gradWeight, workspace, s);
 }
 
+extern "C" int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *mask_or_null, void *y,
+                             void *stream, int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                             int32_t *device_status_or_null)
+{
+    if (!x || !weight || !y)
+        return kErrNull;
+    Plan p;
+    const int32_t st = make_plan(S, B, H, W, dtype, &p);
+    if (st != kOk)
+        return st;
+    if (!aligned16(x) || !aligned16(weight) || !aligned16(y))
+        return kErrInvalid;
+    return launch_fwd(p, x, weight, mask_or_null, y, device_status_or_null,
+                      static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *status_out)
 {
     if (!workspace || !status_out)

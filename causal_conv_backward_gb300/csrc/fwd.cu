@@ -1,0 +1,320 @@
+// fwd.cu - sm_103a kernel of the masked causal depthwise conv1d forward.
+//
+// The forward of the operator whose gradient mcc1d_bwd computes (the CANN
+// page "aclnnMaskedCausalConv1dBackward" names it MaskedCausalConv1d and
+// calls the mask the convolution's output mask): for every channel h,
+//   y(t,j) = mask(j,t) * (w(0)*x(t-2,j) + w(1)*x(t-1,j) + w(2)*x(t,j))
+// with x zero before t = 0. Transposing this map gives exactly the page's
+// gradX and gradWeight formulas.
+//
+// Same streaming design as the backward, with the two-row halo behind each
+// row instead of ahead: per stage the producer warp copies x rows t .. t+R-1
+// (plus t-2, t-1 when a sequence or CTA range starts) into a ring slot with
+// cp.async.bulk and stores the stage's output-mask bytes; consumer threads
+// keep x(t-2), x(t-1) in registers, form y with the compensated three-term
+// sum and a 16-byte streaming store. No reduction, no workspace.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "plan.h"
+
+namespace mcc1d {
+
+constexpr int kFwdR = 8;             // output rows per stage
+constexpr int kFwdMaxThreads = 160;  // 4 consumer warps + producer
+
+struct FwdParams {
+    const uint8_t *x;      // [S,B,H] 16-bit, addressed in bytes
+    const uint16_t *w;     // [3,H]
+    const uint8_t *mask;   // [B,S] or null
+    uint8_t *y;            // [S,B,H]
+    int32_t *status;       // device word or null: set to kErrTimeout if a wait gives up
+    int64_t S, BS, H, N;
+    int32_t B, hb_width, ncta, stages;
+    uint32_t row_bytes, slot_bytes, off_mask, off_bar;
+    int32_t contig_rows;
+};
+
+// Byte q of a stage (row cursor at output row t = c.i): q = 0, 1 say whether
+// the halo rows t-2, t-1 exist (t-2+q >= 0); q >= 2 is the output mask of row
+// t+q-2 (zero past the end of S).
+template <int R>
+__device__ __forceinline__ uint32_t fwd_stage_byte(const FwdParams &p, const Cursor &c, int lane)
+{
+    if (lane < 2)
+        return c.i - 2 + lane >= 0 ? 1u : 0u;
+    if (lane >= R + 2)
+        return 0;
+    const int64_t row = c.i + lane - 2;
+    if (row >= p.S)
+        return 0;
+    if (p.mask == nullptr)
+        return 1;
+    return __ldg(p.mask + (int64_t)c.j * p.S + row) != 0 ? 1u : 0u;
+}
+
+template <int R>
+__device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64_t r1, int lane)
+{
+    const int NS = p.stages;
+    const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
+    const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
+    const uint32_t ring0 = smem_u32(smem);
+    const int64_t row_elems = (int64_t)p.B * p.H;
+    Cursor cur;
+    cur.init(r0, r1, p.S, p.BS);
+    int slot = 0, stage = 0;
+    uint32_t ph = 0;
+    bool dead = false;
+    uint32_t mnext = fwd_stage_byte<R>(p, cur, lane);
+    while (cur.pos < r1) {
+        const int n = cur.rows<R>(p.S);
+        const bool head = (stage == 0) || (cur.i == 0);
+        const uint32_t mcur = mnext;
+        if (stage >= NS) {
+            const bool ok = mbar_wait_bounded(bar_empty0 + 8u * slot, ph ^ 1u);
+            dead = __any_sync(0xFFFFFFFFu, !ok);
+            if (dead)
+                break;
+        }
+        if (lane < R + 2)
+            smem[p.off_mask + 32u * slot + lane] = (uint8_t)mcur;
+        {
+            Cursor nx = cur;
+            nx.advance(n, p.S, p.B);
+            if (nx.pos < r1)
+                mnext = fwd_stage_byte<R>(p, nx, lane);
+        }
+        const int64_t hb0 = (int64_t)cur.hb * p.hb_width;
+        const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
+        const uint32_t wbytes = (uint32_t)width * 2u;
+        // slot row q holds x row t-2+q; the stage loads q in [q0, n+2)
+        int q0 = 2;
+        if (head)
+            q0 = cur.i >= 2 ? 0 : (int)(2 - cur.i);
+        const int nrows = n + 2 - q0;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar_full0 + 8u * slot, (uint32_t)nrows * wbytes);
+        __syncwarp();
+        const uint32_t slot_base = ring0 + (uint32_t)slot * p.slot_bytes;
+        if (p.contig_rows) {
+            if (lane == 0)
+                bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.x + 2 * (cur.i - 2 + q0) * p.H,
+                         (uint32_t)nrows * wbytes, bar_full0 + 8u * slot);
+        } else if (lane < nrows) {
+            const int q = q0 + lane;
+            const int64_t e = (cur.i - 2 + q) * row_elems + (int64_t)cur.j * p.H + hb0;
+            bulk_g2s(slot_base + (uint32_t)q * p.row_bytes, p.x + 2 * e, wbytes, bar_full0 + 8u * slot);
+        }
+        cur.advance(n, p.S, p.B);
+        ++stage;
+        if (++slot == NS) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+    const int used = stage < NS ? stage : NS;
+    for (int s = 0; s < used; ++s) {
+        const int last = s + NS * ((stage - 1 - s) / NS);
+        if (!mbar_wait_bounded(bar_full0 + 8u * s, (uint32_t)((last / NS) & 1)))
+            dead = true;
+    }
+    return __any_sync(0xFFFFFFFFu, dead);
+}
+
+template <int DT, int R, int NP>
+__device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64_t r1, int ct, int lane)
+{
+    constexpr int CH = 2 * NP;
+    const int NS = p.stages;
+    const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
+    const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
+    const int64_t row_stride = 2 * (int64_t)p.B * p.H;
+    Cursor cur;
+    cur.init(r0, r1, p.S, p.BS);
+    int hb_cur = -1;
+    bool active = false;
+    Vf<NP> w0, w1, w2, g0, g1;
+#pragma unroll
+    for (int e = 0; e < NP; ++e)
+        g0.e[e] = g1.e[e] = make_float2(0.f, 0.f);
+    int slot = 0, stage = 0;
+    uint32_t ph = 0;
+    bool dead = false;
+    while (cur.pos < r1) {
+        const int n = cur.rows<R>(p.S);
+        const bool head = (stage == 0) || (cur.i == 0);
+        if (cur.hb != hb_cur) {
+            hb_cur = cur.hb;
+            const int64_t hb0 = (int64_t)hb_cur * p.hb_width;
+            const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
+            active = CH * ct < width;
+            if (active) {
+                w0 = unpack<DT, NP>(ldg_raw<NP>(p.w + 0 * p.H + hb0 + CH * ct));
+                w1 = unpack<DT, NP>(ldg_raw<NP>(p.w + 1 * p.H + hb0 + CH * ct));
+                w2 = unpack<DT, NP>(ldg_raw<NP>(p.w + 2 * p.H + hb0 + CH * ct));
+            }
+        }
+        if (!dead) {
+            const uint32_t bar = bar_full0 + 8u * slot;
+            const bool ok = mbar_try_wait(bar, ph) || mbar_wait_bounded(bar, ph);
+            dead = __any_sync(0xFFFFFFFFu, !ok);
+        }
+        if (!dead && active) {
+            const uint8_t *xs = smem + (size_t)slot * p.slot_bytes + 2 * CH * ct;
+            const uint8_t *ms = smem + p.off_mask + 32u * slot;
+            if (head) {
+                g0 = load_masked<DT, NP>(xs, ms[0]);
+                g1 = load_masked<DT, NP>(xs + p.row_bytes, ms[1]);
+            }
+            uint8_t *yp = p.y + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
+            auto row = [&](int r) {
+                const Vf<NP> g2 = unpack<DT, NP>(load_raw<NP>(xs + (size_t)(r + 2) * p.row_bytes));
+                const uint32_t keep = 0u - (uint32_t)ms[r + 2];
+                uint32_t o[NP];
+#pragma unroll
+                for (int e = 0; e < NP; ++e) {
+                    // products of two 16-bit values are exact in fp32; TwoSum of
+                    // the first two, one more add, then the correction
+                    const float2 p0 = mul2(g0.e[e], w0.e[e]);
+                    const float2 p1 = mul2(g1.e[e], w1.e[e]);
+                    const float2 p2 = mul2(g2.e[e], w2.e[e]);
+                    const float2 s = add2(p0, p1);
+                    const float2 bb = sub2(s, p0);
+                    const float2 err = add2(sub2(p0, sub2(s, bb)), sub2(p1, bb));
+                    const float2 t = add2(s, p2);
+                    o[e] = pack2<DT>(add2(t, err)) & keep;  // output mask
+                }
+                store_cs<NP>(yp + (int64_t)r * row_stride, o);
+                g0 = g1;
+                g1 = g2;
+            };
+            if (n == R) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    row(r);
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (r < n)
+                        row(r);
+            }
+        }
+        __syncwarp();
+        if (!dead && lane == 0)
+            mbar_arrive(bar_empty0 + 8u * slot);
+        cur.advance(n, p.S, p.B);
+        ++stage;
+        if (++slot == NS) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+    return dead;
+}
+
+template <int DT, int R, int NP>
+__global__ void __launch_bounds__(kFwdMaxThreads) mcc1d_fwd_main(const __grid_constant__ FwdParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_err;
+    const int c = blockIdx.x;
+    const int64_t r0 = cta_row_begin(c, p.N, p.ncta);
+    const int64_t r1 = cta_row_begin(c + 1, p.N, p.ncta);
+    const int consumer_warps = (int)(blockDim.x >> 5) - 1;
+    if (threadIdx.x == 0) {
+        s_err = 0;
+        const uint32_t bar0 = smem_u32(smem + p.off_bar);
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(bar0 + 8u * s, 1);
+            mbar_init(bar0 + 8u * (p.stages + s), (uint32_t)consumer_warps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    bool dead;
+    if (threadIdx.x < 32)
+        dead = fwd_produce<R>(p, smem, r0, r1, lane);
+    else
+        dead = fwd_consume<DT, R, NP>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
+    if (dead && lane == 0)
+        atomicOr(&s_err, 1);
+    __syncthreads();
+    if (threadIdx.x == 0 && s_err && p.status != nullptr)
+        atomicOr(p.status, kErrTimeout);
+}
+
+typedef void (*FwdFn)(FwdParams);
+
+static FwdFn fwd_kernel(int dtype, int vec)
+{
+    if (dtype == 0)
+        return vec == 4 ? mcc1d_fwd_main<0, kFwdR, 2> : mcc1d_fwd_main<0, kFwdR, 4>;
+    return vec == 4 ? mcc1d_fwd_main<1, kFwdR, 2> : mcc1d_fwd_main<1, kFwdR, 4>;
+}
+
+int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint8_t *mask, void *y,
+                   int32_t *status, cudaStream_t stream)
+{
+    // Same CTA partition as the backward; the ring holds x rows only.
+    FwdParams fp;
+    fp.x = static_cast<const uint8_t *>(x);
+    fp.w = static_cast<const uint16_t *>(weight);
+    fp.mask = mask;
+    fp.y = static_cast<uint8_t *>(y);
+    fp.status = status;
+    fp.S = pl.S;
+    fp.BS = pl.B * pl.S;
+    fp.H = pl.H;
+    fp.N = pl.rows_total;
+    fp.B = (int32_t)pl.B;
+    fp.hb_width = pl.hb_width;
+    fp.ncta = pl.ncta;
+    fp.row_bytes = pl.row_bytes;
+    fp.slot_bytes = (uint32_t)(kFwdR + 2) * pl.row_bytes;
+    const int64_t budget = kSmemPerSM / pl.ctas_per_sm - kSmemReservedPerCta - 64;
+    int64_t ns = budget / (fp.slot_bytes + 48);
+    if (ns > 8)
+        ns = 8;
+    if (ns < 2)
+        ns = 2;
+    fp.stages = (int32_t)ns;
+    fp.off_mask = (uint32_t)ns * fp.slot_bytes;
+    fp.off_bar = (fp.off_mask + 32u * (uint32_t)ns + 15u) & ~15u;
+    const uint32_t smem = fp.off_bar + 16u * (uint32_t)ns;
+    fp.contig_rows = (pl.B == 1 && pl.n_hb == 1) ? 1 : 0;
+
+    FwdFn fn = fwd_kernel(pl.dtype, pl.vec);
+    static std::atomic<uint64_t> done[4];
+    const int slot_id = pl.dtype * 2 + (pl.vec == 4 ? 1 : 0);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return kErrCuda;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(done[slot_id].load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemPerCtaMax - 1024) != cudaSuccess)
+            return kErrCuda;
+        done[slot_id].fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.ncta);
+    cfg.blockDim = dim3((unsigned)pl.threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    if (cudaLaunchKernelEx(&cfg, fn, fp) != cudaSuccess)
+        return kErrCuda;
+    return kOk;
+}
+
+}  // namespace mcc1d

@@ -40,12 +40,12 @@
 
 #include <atomic>
 
+#include "device_common.cuh"
 #include "launch.h"
 #include "plan.h"
 
 namespace mcc1d {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kMaxThreads = 160;                  // 4 consumer warps + producer
 
 struct MainParams {
@@ -74,246 +74,6 @@ struct ReduceParams {
     int64_t H;
     int32_t hb_width, ncta, nchunk;
     int32_t c_lo[kMaxHb], c_hi[kMaxHb], slot_base[kMaxHb];
-};
-
-// ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits for the phase of `bar` with the given parity to complete; gives up
-// (returns false) after kWaitLimitNs.
-__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs)
-            return false;
-    }
-}
-
-// Global -> shared bulk copy completing on an mbarrier (no multicast).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// Packed fp32x2 arithmetic (sm_100+), each lane rounded to nearest even.
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\t"
-        "mov.b64 rb, {%4, %5};\n\t"
-        "sub.rn.f32x2 rd, ra, rb;\n\t"
-        "mov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-// ------------------------------------------------------------------ 16-bit types
-// DT 0 = bf16, 1 = fp16. A consumer thread owns 2*NP channels: NP = 4 moves
-// 16 bytes per row (uint4), NP = 2 moves 8 bytes (uint2).
-template <int NP>
-struct Vf {
-    float2 e[NP];
-};
-
-template <int NP>
-struct Raw {
-    uint32_t u[NP];
-};
-
-template <int DT>
-__device__ __forceinline__ float2 unpack2(uint32_t u)
-{
-    if (DT == 0) {
-        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-    } else {
-        union {
-            uint32_t u;
-            __half2 h;
-        } c;
-        c.u = u;
-        return __half22float2(c.h);
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ uint32_t pack2(float2 v)
-{
-    if (DT == 0) {
-        union {
-            __nv_bfloat162 b;
-            uint32_t u;
-        } c;
-        c.b = __floats2bfloat162_rn(v.x, v.y);
-        return c.u;
-    } else {
-        union {
-            __half2 h;
-            uint32_t u;
-        } c;
-        c.h = __floats2half2_rn(v.x, v.y);
-        return c.u;
-    }
-}
-
-// Plain vector load (shared or global memory).
-template <int NP>
-__device__ __forceinline__ Raw<NP> load_raw(const void *p)
-{
-    Raw<NP> r;
-    if (NP == 4) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(p);
-        r.u[0] = v.x;
-        r.u[1] = v.y;
-        r.u[2] = v.z;
-        r.u[3] = v.w;
-    } else {
-        const uint2 v = *reinterpret_cast<const uint2 *>(p);
-        r.u[0] = v.x;
-        r.u[1] = v.y;
-    }
-    return r;
-}
-
-// Read-only global load through the non-coherent path.
-template <int NP>
-__device__ __forceinline__ Raw<NP> ldg_raw(const void *p)
-{
-    Raw<NP> r;
-    if (NP == 4) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
-        r.u[0] = v.x;
-        r.u[1] = v.y;
-        r.u[2] = v.z;
-        r.u[3] = v.w;
-    } else {
-        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
-        r.u[0] = v.x;
-        r.u[1] = v.y;
-    }
-    return r;
-}
-
-// Streaming (evict-first) global store.
-template <int NP>
-__device__ __forceinline__ void store_cs(void *p, const uint32_t (&u)[NP])
-{
-    if (NP == 4)
-        __stcs(reinterpret_cast<uint4 *>(p), make_uint4(u[0], u[1], u[2], u[3]));
-    else
-        __stcs(reinterpret_cast<uint2 *>(p), make_uint2(u[0], u[1]));
-}
-
-template <int DT, int NP>
-__device__ __forceinline__ Vf<NP> unpack(const Raw<NP> &r)
-{
-    Vf<NP> v;
-#pragma unroll
-    for (int e = 0; e < NP; ++e)
-        v.e[e] = unpack2<DT>(r.u[e]);
-    return v;
-}
-
-// A staged gradY row, masked by clearing the bits (exact +0 whatever the
-// staged bytes hold; rows past the end of S carry a zero mask byte).
-template <int DT, int NP>
-__device__ __forceinline__ Vf<NP> load_masked(const uint8_t *p, uint8_t keep_byte)
-{
-    Raw<NP> r = load_raw<NP>(p);
-    const uint32_t keep = 0u - (uint32_t)keep_byte;
-#pragma unroll
-    for (int e = 0; e < NP; ++e)
-        r.u[e] &= keep;
-    return unpack<DT, NP>(r);
-}
-
-// ------------------------------------------------------------------ row cursor
-// Position in the flattened (hb, j, i) row sequence of one CTA range.
-struct Cursor {
-    int64_t pos, end, i;
-    int32_t j, hb;
-
-    __device__ __forceinline__ void init(int64_t r0, int64_t r1, int64_t S, int64_t BS)
-    {
-        pos = r0;
-        end = r1;
-        hb = (int32_t)(r0 / BS);
-        const int64_t rem = r0 - (int64_t)hb * BS;
-        j = (int32_t)(rem / S);
-        i = rem - (int64_t)j * S;
-    }
-    // Rows of the next stage: at most R, never across a sequence end or the range end.
-    template <int R>
-    __device__ __forceinline__ int rows(int64_t S) const
-    {
-        int64_t n = S - i;
-        if (end - pos < n)
-            n = end - pos;
-        return n < R ? (int)n : R;
-    }
-    __device__ __forceinline__ void advance(int n, int64_t S, int32_t B)
-    {
-        pos += n;
-        i += n;
-        if (i == S) {
-            i = 0;
-            if (++j == B) {
-                j = 0;
-                ++hb;
-            }
-        }
-    }
 };
 
 // ------------------------------------------------------------------ producer

@@ -21,4 +21,9 @@ int32_t launch_bwd(const Plan &p, const Layout &L, const void *gradY, const void
 int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_t S, int64_t B,
                     int64_t H, cudaStream_t stream);
 
+// Enqueues the forward kernel of plan `p` (dense tensors). `status` is a
+// device word the kernel ORs kErrTimeout into if a wait gives up, or null.
+int32_t launch_fwd(const Plan &p, const void *x, const void *weight, const uint8_t *mask, void *y,
+                   int32_t *status, cudaStream_t stream);
+
 }  // namespace mcc1d

@@ -67,6 +67,12 @@ class Workload:
         has_mask = self.mask[0] != "none"
         return 6 * self.E + (self.B * self.S if has_mask else 0) + 2 * 2 * self.W * self.H
 
+    def fwd_algorithmic_bytes(self) -> int:
+        """Minimum HBM bytes of one forward call: read x and write y (2 B each
+        per element), read the mask (1 B per token, if any) and the weight."""
+        has_mask = self.mask[0] != "none"
+        return 4 * self.E + (self.B * self.S if has_mask else 0) + 2 * self.W * self.H
+
     def without_mask(self) -> "Workload":
         return replace(self, name=self.name + "_nomask", mask=("none",))
 

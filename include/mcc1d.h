@@ -224,6 +224,31 @@ int32_t mcc1d_bwd_noalloc(const void *gradY, const void *x, const void *weight,
                           void *stream, int64_t S, int64_t B, int64_t H, int64_t W,
                           int32_t dtype);
 
+/*
+ * Forward of the same operator (MaskedCausalConv1d, the forward the page
+ * names; its mask is the convolution's output mask): for every channel h,
+ *
+ *   y(t,j,h) = mask(j,t) * sum over k = 0..W-1 of weight(k,h) * x(t-W+1+k, j, h)
+ *
+ * with x zero before t = 0, a causal depthwise convolution with W-1 positions
+ * of left padding. mcc1d_bwd computes exactly the gradients of this map. The
+ * page prints no forward API; this one follows mcc1d_bwd's conventions:
+ *
+ *   x            [S,B,H] input, dtype, dense, 16-byte aligned
+ *   weight       [W,H]   input, dtype, dense, 16-byte aligned
+ *   mask_or_null [B,S]   input bytes, nonzero = keep; NULL keeps every position
+ *   y            [S,B,H] output, dtype, dense, 16-byte aligned; every element written
+ *   device_status_or_null  a device int32 the kernel sets to
+ *                MCC1D_ERR_DEVICE_TIMEOUT if a bounded device-side wait gives
+ *                up (it is never cleared: zero it before the call to use it), or NULL
+ *
+ * Enqueued on `stream`; no workspace; deterministic; y within 1 ulp of the
+ * exact value rounded once. Errors and shape limits as mcc1d_bwd.
+ */
+int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *mask_or_null, void *y,
+                  void *stream, int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                  int32_t *device_status_or_null);
+
 /* Static text for a status code; never NULL. */
 const char *mcc1d_status_string(int32_t status);
 

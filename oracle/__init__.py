@@ -75,7 +75,7 @@ class Oracle:
         lib.mcc1d_oracle_gradx_at.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp,
                                               i64, vp, vp, vp]
         lib.mcc1d_oracle_gradx_at.restype = i32
-        lib.mcc1d_oracle_fwd.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp]
+        lib.mcc1d_oracle_fwd.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, i32]
         lib.mcc1d_oracle_fwd.restype = i32
         self.lib = lib
         self.path = lib_path
@@ -136,14 +136,23 @@ class Oracle:
             raise ValueError("oracle rejected its arguments")
         return bits, exact
 
-    def fwd(self, S, B, H, W, dtype, x, w, mask=None) -> np.ndarray:
+    def fwd(self, S, B, H, W, dtype, x, w, mask=None, *, nthreads: int = 0) -> np.ndarray:
         """The forward y = mask * causal depthwise conv(x, w), fp64 [S,B,H]."""
         y = np.empty((S, B, H), np.float64)
         rc = self.lib.mcc1d_oracle_fwd(S, B, H, W, _dt(dtype), _ptr(x), _ptr(w), _ptr(mask),
-                                       _ptr(y))
+                                       _ptr(y), None, nthreads)
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return y
+
+    def fwd_bits(self, S, B, H, W, dtype, x, w, mask=None, *, nthreads: int = 0) -> np.ndarray:
+        """The forward rounded once to the 16-bit type, uint16 [S,B,H]."""
+        yb = np.empty((S, B, H), np.uint16)
+        rc = self.lib.mcc1d_oracle_fwd(S, B, H, W, _dt(dtype), _ptr(x), _ptr(w), _ptr(mask),
+                                       None, _ptr(yb), nthreads)
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return yb
 
 
 _lock = threading.Lock()
@@ -189,3 +198,7 @@ def gradx_at(*a, **k):
 
 def fwd(*a, **k):
     return get().fwd(*a, **k)
+
+
+def fwd_bits(*a, **k):
+    return get().fwd_bits(*a, **k)

@@ -272,36 +272,47 @@ int mcc1d_oracle_gradx_at(int64_t S, int64_t B, int64_t H, int64_t W, int dtype,
 }
 
 /*
- * The forward pass that this backward differentiates, used only by the
- * oracle's own checks (adjoint identity, brute-force Jacobian). The page
- * names the forward operator (MaskedCausalConv1d) but prints only the
- * backward; transposing the two backward formulas gives
+ * The forward pass that this backward differentiates. The page names the
+ * forward operator (MaskedCausalConv1d) but prints only the backward;
+ * transposing the two backward formulas gives
  *
  *   y(t,j,h) = mask(j,t) * sum over k=0..W-1 of weight(k,h) * x(t-(W-1)+k, j, h)
  *
  * with x zero at negative S indices: a causal depthwise convolution with W-1
  * positions of left padding and the mask on its output (the parameter table
  * describes the mask as the convolution's output mask).
- * y: [S,B,H] fp64.
+ * Outputs (either may be NULL): y [S,B,H] fp64, y_bits [S,B,H] the same
+ * values rounded once to the 16-bit type.
  */
 int mcc1d_oracle_fwd(int64_t S, int64_t B, int64_t H, int64_t W, int dtype,
-                     const uint16_t *x, const uint16_t *w, const uint8_t *mask, double *y)
+                     const uint16_t *x, const uint16_t *w, const uint8_t *mask, double *y,
+                     uint16_t *y_bits, int nthreads)
 {
-    if (S < 1 || B < 1 || H < 1 || W < 1 || !x || !w || !y)
+    if (S < 1 || B < 1 || H < 1 || W < 1 || !x || !w || (!y && !y_bits))
         return -1;
-    for (int64_t t = 0; t < S; ++t)
-        for (int64_t j = 0; j < B; ++j) {
-            double m = mask ? (mask[j * S + t] ? 1.0 : 0.0) : 1.0;
-            for (int64_t h = 0; h < H; ++h) {
-                double acc = 0.0;
-                for (int64_t k = 0; k < W; ++k) {
-                    int64_t s = t - (W - 1) + k;
-                    if (s >= 0)
-                        acc += mcc1d_oracle_to_double(w[k * H + h], dtype) *
-                               mcc1d_oracle_to_double(x[(s * B + j) * H + h], dtype);
-                }
-                y[(t * B + j) * H + h] = m * acc;
+    double *tab = decode_table(dtype);
+    if (!tab)
+        return -1;
+    int nt = set_threads(nthreads);
+    int64_t rows = S * B;
+#pragma omp parallel for schedule(static) num_threads(nt)
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t t = r / B, j = r % B;
+        double m = mask ? (mask[j * S + t] ? 1.0 : 0.0) : 1.0;
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < W; ++k) {
+                int64_t s = t - (W - 1) + k;
+                if (s >= 0)
+                    acc += tab[w[k * H + h]] * tab[x[(s * B + j) * H + h]];
             }
+            int64_t o = (t * B + j) * H + h;
+            if (y)
+                y[o] = m * acc;
+            if (y_bits)
+                y_bits[o] = mcc1d_oracle_from_double(m * acc, dtype);
         }
+    }
+    free(tab);
     return 0;
 }

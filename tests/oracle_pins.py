@@ -334,6 +334,24 @@ def pin_forward_torch(orc):
             assert np.allclose(y, yt, rtol=0, atol=1e-12 * (np.abs(yt).max() + 1)), (dt, S, B, H, W)
 
 
+def pin_forward_rounding(orc):
+    """The rounded forward is the fp64 forward rounded once: for fp16 against
+    numpy's double -> half rounding, for bf16 against the (separately pinned)
+    converter; masked rows are exactly zero."""
+    rng = np.random.default_rng(43)
+    for dt in ("bf16", "fp16"):
+        S, B, H = 33, 3, 16
+        x, w = rand_bits(rng, (S, B, H), dt), rand_bits(rng, (3, H), dt)
+        mask = (rng.random((B, S)) < 0.7).astype(np.uint8)
+        y = orc.fwd(S, B, H, 3, dt, x, w, mask)
+        yb = orc.fwd_bits(S, B, H, 3, dt, x, w, mask)
+        if dt == "fp16":
+            assert np.array_equal(dec(yb, dt), dec(y.astype(np.float16).view(np.uint16), dt))
+        else:
+            assert np.array_equal(yb, orc.encode(y, dt))
+        assert np.all(dec(yb, dt)[(mask.T == 0)] == 0)
+
+
 # ---------------------------------------------------------------- conversions
 def pin_converters(orc):
     """Decoding every 16-bit pattern, and rounding doubles to 16 bits (ties to
@@ -387,4 +405,4 @@ def pin_gradx_at(orc):
 
 ALL_PINS = [pin_golden, pin_closed_form_ones, pin_shift_identities, pin_mask_special_cases,
             pin_s1, pin_batch_independence, pin_jacobian_bruteforce, pin_adjoint_identity,
-            pin_torch_autograd, pin_forward_torch, pin_converters, pin_gradx_at]
+            pin_torch_autograd, pin_forward_torch, pin_forward_rounding, pin_converters, pin_gradx_at]

@@ -163,3 +163,17 @@ def test_ex_rejects(lib):
     assert call(ctypes.byref(t), 64, 2, 384, 3, 0, None, need, None) == NULLPTR
     assert call(ctypes.byref(t), 64, 2, 384, 3, 0, 0x70008, need, None) == INVALID
     assert call(ctypes.byref(t), 64, 2, 384, 3, 0, 0x70000, need - 1, None) == WORKSPACE
+
+
+def test_fwd_rejects_before_any_launch(lib):
+    f = m.load().mcc1d_fwd
+    ok = dict(x=0x1000, w=0x2000, y=0x3000)
+
+    def call(S=64, B=2, H=384, W=3, dt=0, **kw):
+        a = {**ok, **kw}
+        return f(a["x"], a["w"], None, a["y"], None, S, B, H, W, dt, None)
+
+    assert call(x=None) == NULLPTR and call(y=None) == NULLPTR and call(w=None) == NULLPTR
+    assert call(x=0x1008) == INVALID and call(y=0x3002) == INVALID
+    assert call(dt=2) == INVALID
+    assert call(B=0) == SHAPE and call(H=4000) == SHAPE and call(W=5) == SHAPE
