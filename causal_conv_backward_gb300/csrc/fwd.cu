@@ -27,7 +27,8 @@
 namespace mcc1d {
 
 constexpr int kFwdR = 8;             // output rows per stage
-constexpr int kFwdMaxThreads = 160;  // 4 consumer warps + producer
+constexpr int kFwdMaxThreads = 288;  // 8 consumer warps + producer
+constexpr int kFwdMaxStages = 8;
 
 struct FwdParams {
     const uint8_t *x;      // [S,B,H] 16-bit, addressed in bytes
@@ -283,8 +284,8 @@ int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint
     fp.slot_bytes = (uint32_t)(kFwdR + 2) * pl.row_bytes;
     const int64_t budget = kSmemPerSM / pl.ctas_per_sm - kSmemReservedPerCta - 64;
     int64_t ns = budget / (fp.slot_bytes + 48);
-    if (ns > 8)
-        ns = 8;
+    if (ns > kFwdMaxStages)
+        ns = kFwdMaxStages;
     if (ns < 2)
         ns = 2;
     fp.stages = (int32_t)ns;

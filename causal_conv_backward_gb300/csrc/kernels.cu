@@ -46,7 +46,7 @@
 
 namespace mcc1d {
 
-constexpr int kMaxThreads = 160;                  // 4 consumer warps + producer
+constexpr int kMaxThreads = 288;                  // 8 consumer warps + producer
 
 struct MainParams {
     const uint8_t *gy;     // [S,B,H] 16-bit elements, addressed in bytes

@@ -26,6 +26,15 @@ int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype
 
 int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p)
 {
+    const int32_t st = make_plan_for(S, B, H, W, dtype, 8, kHbWidthWide, p);
+    if (st != kOk || p->rows_total / p->ncta >= kWideMinRowsPerCta)
+        return st;
+    return make_plan_for(S, B, H, W, dtype, 8, kHbWidthNarrow, p);
+}
+
+int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                      int target_consumer_warps, int max_hb_width, Plan *p)
+{
     int32_t st = validate_shape(S, B, H, W, dtype);
     if (st != kOk)
         return st;
@@ -35,9 +44,9 @@ int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Pla
     p->H = H;
     p->dtype = dtype;
 
-    // H-blocks: as few as possible of at most 1024 halves, balanced, each a
-    // multiple of 64 halves so every staged row is a multiple of 128 bytes.
-    p->n_hb = (int32_t)ceil_div(H, kMaxHbWidth);
+    // H-blocks: as few as possible of at most max_hb_width halves, balanced,
+    // each a multiple of 64 halves so every staged row is a multiple of 128 bytes.
+    p->n_hb = (int32_t)ceil_div(H, max_hb_width);
     p->hb_width = (int32_t)round_up(ceil_div(H, p->n_hb), 64);
     // Channels per consumer thread: 8 (16-byte vectors), or 4 when 16-byte
     // vectors would leave part of the last warp idle and 8-byte vectors fill
@@ -49,8 +58,8 @@ int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Pla
     p->consumer_warps = (int32_t)ceil_div(vectors, 32);
     p->threads = 32 * (p->consumer_warps + 1);
 
-    // Aim for at least 8 consumer warps per SM.
-    int cps = (int)ceil_div(8, p->consumer_warps);
+    // Aim for at least target_consumer_warps consumer warps per SM.
+    int cps = (int)ceil_div(target_consumer_warps, p->consumer_warps);
     while (cps > 1 && cps * p->threads > 2048)
         --cps;
     p->ctas_per_sm = cps;

@@ -21,7 +21,9 @@ constexpr int kSmemPerSM = 233472;    // 228 KB of shared memory per SM
 constexpr int kSmemPerCtaMax = 232448;// 227 KB opt-in maximum per CTA
 constexpr int kSmemReservedPerCta = 1024;
 constexpr int kMaxHb = 64;            // upper bound on H-blocks recorded in a plan
-constexpr int kMaxHbWidth = 1024;     // halves per H-block (2 KB rows)
+constexpr int kHbWidthNarrow = 1024;  // halves per H-block: 2 KB rows
+constexpr int kHbWidthWide = 2048;    // 4 KB rows, for long CTA ranges
+constexpr int kWideMinRowsPerCta = 1024;
 constexpr int kMinRowsPerCta = 16;    // below this a CTA is not worth its pipeline fill
 constexpr int kFlushStages = 16;      // stages between register -> shared accumulator flushes
 constexpr int kReduceLanes = 8;       // float4 column groups per reduce CTA (32 columns)
@@ -101,7 +103,13 @@ inline Layout dense_layout(int64_t S, int64_t B, int64_t H)
 int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype);
 
 // Fills *p for a valid shape; returns the validate_shape status otherwise.
+// make_plan is the backward's plan: 8 consumer warps per SM (its register
+// budget), and 4 KB H-block rows when every CTA range is long enough for the
+// larger copies to pay, else 2 KB. make_plan_for fixes both choices (the
+// forward, at about 96 registers a thread, asks for more warps).
 int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p);
+int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                      int target_consumer_warps, int max_hb_width, Plan *p);
 
 // First row of CTA c's range.
 MCC1D_HD inline int64_t cta_row_begin(int64_t c, int64_t rows_total, int64_t ncta) {

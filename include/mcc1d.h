@@ -203,7 +203,7 @@ int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *st
  *
  *  - A shape whose mcc1d_bwd_workspace_size exceeds MCC1D_NOALLOC_SCRATCH_BYTES
  *    is rejected with MCC1D_ERR_WORKSPACE before anything is enqueued. Every
- *    shape within the limits above needs at most about 4.2 MB, so all of them
+ *    shape within the limits above needs at most about 6.7 MB, so all of them
  *    fit; the check guards against a future plan needing more.
  *  - All calls on a device share the one array. Calls that may overlap on the
  *    GPU (different streams, or host threads with no ordering between them)
