@@ -63,6 +63,8 @@ def load():
         lib.mcc1d_bwd_ex_workspace_size.restype = i32
         lib.mcc1d_bwd_ex.argtypes = [ctypes.POINTER(Mcc1dTensors), i64, i64, i64, i64, i32, vp, u64, vp]
         lib.mcc1d_bwd_ex.restype = i32
+        lib.mcc1d_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, u64]
+        lib.mcc1d_bwd_host.restype = i32
         lib.mcc1d_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, vp]
         lib.mcc1d_fwd.restype = i32
         lib.mcc1d_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32]
@@ -145,6 +147,19 @@ def mcc1d_bwd_ex(t: Mcc1dTensors, S, B, H, W, dtype, workspace, workspace_bytes,
                              int(workspace_bytes), stream or None)
     if st != 0:
         raise Mcc1dError(st, "mcc1d_bwd_ex")
+
+
+def mcc1d_bwd_host(gradY, x, weight, mask_or_null, gradX, gradWeight, workspace, stream,
+                   S, B, H, W, dtype, workspace_bytes) -> None:
+    """Enqueue the backward on tensors that may be page-locked host buffers
+    (e.g. torch tensors made with pin_memory=True); workspace on the device."""
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = load().mcc1d_bwd_host(_ptr(gradY), _ptr(x), _ptr(weight), _ptr(mask_or_null), _ptr(gradX),
+                               _ptr(gradWeight), _ptr(workspace), stream or None, S, B, H, W,
+                               dtype_code(dtype), int(workspace_bytes))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_bwd_host")
 
 
 def mcc1d_fwd(x, weight, mask_or_null, y, stream, S, B, H, W, dtype, device_status=None) -> None:

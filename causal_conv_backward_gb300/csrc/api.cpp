@@ -53,6 +53,52 @@ extern "C" int32_t mcc1d_bwd(const void *gradY, const void *x, const void *weigh
 
 namespace {
 
+// Device address of a pointer the current device can access: device memory,
+// managed memory, or page-locked host memory. Null when it cannot.
+void *device_address(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeUnregistered)
+        return nullptr;
+    int dev = -1;
+    if (a.type == cudaMemoryTypeDevice && (cudaGetDevice(&dev) != cudaSuccess || dev != a.device))
+        return nullptr;
+    return a.devicePointer;
+}
+
+}  // namespace
+
+extern "C" int32_t mcc1d_bwd_host(const void *gradY, const void *x, const void *weight,
+                                  const uint8_t *mask_or_null, void *gradX, void *gradWeight,
+                                  void *workspace, void *stream, int64_t S, int64_t B, int64_t H,
+                                  int64_t W, int32_t dtype, uint64_t workspace_bytes)
+{
+    if (!gradY || !x || !weight || !gradX || !gradWeight || !workspace)
+        return kErrNull;
+    Plan p;
+    const int32_t st = make_plan(S, B, H, W, dtype, &p);
+    if (st != kOk)
+        return st;
+    if (!aligned16(gradY) || !aligned16(x) || !aligned16(weight) || !aligned16(gradX) ||
+        !aligned16(gradWeight) || !aligned16(workspace))
+        return kErrInvalid;
+    if (workspace_bytes < p.ws_bytes)
+        return kErrWorkspace;
+    const void *gy_d = device_address(gradY), *x_d = device_address(x), *w_d = device_address(weight);
+    void *gx_d = device_address(gradX), *gw_d = device_address(gradWeight);
+    const void *m_d = mask_or_null ? device_address(mask_or_null) : nullptr;
+    if (!gy_d || !x_d || !w_d || !gx_d || !gw_d || (mask_or_null && !m_d))
+        return kErrInvalid;
+    return launch_direct(p, gy_d, x_d, w_d, static_cast<const uint8_t *>(m_d), gx_d, gw_d, workspace,
+                         static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
 // Plan of a strided call: which inputs are gathered into the workspace first,
 // and where.
 struct ExPlan {

@@ -534,6 +534,39 @@ static bool ensure_smem_attr(const void *fn, int slot_id)
     return true;
 }
 
+int32_t launch_reduce(const Plan &pl, void *workspace, void *gradWeight, cudaStream_t stream)
+{
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    ReduceParams rp;
+    rp.part = reinterpret_cast<const float *>(ws + pl.ws_part_off);
+    rp.status = reinterpret_cast<const int32_t *>(ws + pl.ws_status_off);
+    rp.header = reinterpret_cast<int32_t *>(ws);
+    rp.gw = static_cast<uint8_t *>(gradWeight);
+    rp.H = pl.H;
+    rp.hb_width = pl.hb_width;
+    rp.ncta = pl.ncta;
+    rp.nchunk = (pl.hb_width + kReduceCols - 1) / kReduceCols;
+    for (int h = 0; h < kMaxHb; ++h) {
+        rp.c_lo[h] = pl.c_lo[h];
+        rp.c_hi[h] = pl.c_hi[h];
+        rp.slot_base[h] = pl.slot_base[h];
+    }
+    ReduceFn rfn = pl.dtype == 0 ? mcc1d_bwd_reduce<0> : mcc1d_bwd_reduce<1>;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t rcfg = {};
+    rcfg.gridDim = dim3((unsigned)pl.reduce_blocks);
+    rcfg.blockDim = dim3(kReduceSplits * kReduceLanes);
+    rcfg.dynamicSmemBytes = 0;
+    rcfg.stream = stream;
+    rcfg.attrs = attr;
+    rcfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&rcfg, rfn, rp) != cudaSuccess)
+        return kErrCuda;
+    return kOk;
+}
+
 int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_t S, int64_t B,
                     int64_t H, cudaStream_t stream)
 {
@@ -588,24 +621,8 @@ int32_t launch_bwd(const Plan &pl, const Layout &L, const void *gradY, const voi
     mp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && L.gy[0] == pl.H && L.x[0] == pl.H) ? 1 : 0;
     mp.w_vec = (L.w[1] == 1 && (L.w[0] * 2) % 16 == 0 && ((uintptr_t)weight & 15u) == 0) ? 1 : 0;
 
-    ReduceParams rp;
-    rp.part = mp.part;
-    rp.status = mp.status;
-    rp.header = reinterpret_cast<int32_t *>(ws);
-    rp.gw = static_cast<uint8_t *>(gradWeight);
-    rp.H = pl.H;
-    rp.hb_width = pl.hb_width;
-    rp.ncta = pl.ncta;
-    rp.nchunk = (pl.hb_width + kReduceCols - 1) / kReduceCols;
-    for (int h = 0; h < kMaxHb; ++h) {
-        rp.c_lo[h] = pl.c_lo[h];
-        rp.c_hi[h] = pl.c_hi[h];
-        rp.slot_base[h] = pl.slot_base[h];
-    }
-
     const int R = pl.rows_per_stage;
     MainFn mfn = main_kernel(pl.dtype, R, pl.vec);
-    ReduceFn rfn = pl.dtype == 0 ? mcc1d_bwd_reduce<0> : mcc1d_bwd_reduce<1>;
     if (!mfn)
         return kErrCuda;
     const int attr_slot = (pl.dtype * 2 + (pl.vec == 4 ? 1 : 0)) * 4 + (R == 4 ? 0 : R == 6 ? 1 : 2);
@@ -620,19 +637,7 @@ int32_t launch_bwd(const Plan &pl, const Layout &L, const void *gradY, const voi
     if (cudaLaunchKernelEx(&cfg, mfn, mp) != cudaSuccess)
         return kErrCuda;
 
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t rcfg = {};
-    rcfg.gridDim = dim3((unsigned)pl.reduce_blocks);
-    rcfg.blockDim = dim3(kReduceSplits * kReduceLanes);
-    rcfg.dynamicSmemBytes = 0;
-    rcfg.stream = stream;
-    rcfg.attrs = attr;
-    rcfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&rcfg, rfn, rp) != cudaSuccess)
-        return kErrCuda;
-    return kOk;
+    return launch_reduce(pl, workspace, gradWeight, stream);
 }
 
 }  // namespace mcc1d

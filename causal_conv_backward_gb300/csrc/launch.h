@@ -16,6 +16,18 @@ int32_t launch_bwd(const Plan &p, const Layout &L, const void *gradY, const void
                    const void *weight, const uint8_t *mask, void *gradX, void *gradWeight,
                    void *workspace, cudaStream_t stream);
 
+// Enqueues the reduce kernel of plan `p` (programmatic dependent launch after
+// the main kernel on `stream`): sums the partials in `workspace` and writes
+// gradWeight (any device-accessible address). Returns kOk or kErrCuda.
+int32_t launch_reduce(const Plan &p, void *workspace, void *gradWeight, cudaStream_t stream);
+
+// Enqueues the backward on dense tensors that may live in page-locked host
+// memory (read and written in place by the kernel), then the reduce. Pointers
+// are device-accessible addresses. Returns kOk or kErrCuda.
+int32_t launch_direct(const Plan &p, const void *gradY, const void *x, const void *weight,
+                      const uint8_t *mask, void *gradX, void *gradWeight, void *workspace,
+                      cudaStream_t stream);
+
 // Enqueues a gather of a strided 16-bit [S,B,H] tensor into a dense one
 // (dst 16-byte aligned). Returns kOk or kErrCuda.
 int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_t S, int64_t B,

@@ -125,6 +125,27 @@ int32_t mcc1d_bwd(const void *gradY, const void *x, const void *weight,
                   uint64_t workspace_bytes);
 
 /*
+ * The backward on tensors that may live in host memory (an extension of the
+ * page's call, which takes device tensors). gradY, x, weight, mask, gradX and
+ * gradWeight may each be page-locked host memory (cudaMallocHost,
+ * cudaHostAlloc or cudaHostRegister) or device memory of the current device;
+ * the kernel reads and writes them in place over the host link, so the
+ * inputs stream in, gradX streams out and the arithmetic runs at the same
+ * time, with no staging copies. The workspace is device memory, sized by
+ * mcc1d_bwd_workspace_size. Arguments, layouts, results (within the same
+ * tolerances; gradWeight may differ from mcc1d_bwd in its last bit, its
+ * partial sums are grouped differently) and errors are those of mcc1d_bwd,
+ * plus MCC1D_ERR_PARAM_INVALID for a pointer the device cannot access
+ * (pageable host memory, or memory of another device). Host buffers must
+ * stay valid and untouched until the call completes on `stream`.
+ */
+int32_t mcc1d_bwd_host(const void *gradY, const void *x, const void *weight,
+                       const uint8_t *mask_or_null, void *gradX, void *gradWeight,
+                       void *workspace, void *stream,
+                       int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                       uint64_t workspace_bytes);
+
+/*
  * Tensors of one call with explicit strides: the page's inputs may be
  * non-contiguous (the 非连续Tensor column of its parameter table), its
  * outputs may not. Strides count ELEMENTS for the 16-bit tensors and BYTES for
