@@ -42,7 +42,8 @@ CPU_SAMPLE_S = 4096       # cpu_baseline: first 4096 positions of every batch (a
 REF_SAMPLE_S = 64         # --impl reference: first 64 positions per step
 E2E_STEPS = 10
 PROFILE = os.path.join(ROOT, "profiles", "mcc1d_bwd_main_s16384_b32_h4096_fp16_traffic.txt")
-KERNEL_SRC = os.path.join(ROOT, "causal_conv_backward_gb300", "csrc", "kernels.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "causal_conv_backward_gb300", "csrc", f)
+               for f in ("kernels.cu", "bwd_main.cuh", "device_common.cuh", "plan.cpp", "plan.h")]
 
 
 def parse_args(argv=None):
@@ -57,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", choices=["bwd", "fwd"], default="bwd",
                     help="fwd: time the forward kernel (mcc1d_fwd) on the same workload")
+    ap.add_argument("--W", type=int, default=3,
+                    help="kernel width; other than 3 runs through the strided call mcc1d_bwd_ex")
     ap.add_argument("--layout", choices=["sbh", "bsh"], default="sbh",
                     help="bsh: gradY and x live as [B,S,H] buffers seen as [S,B,H] (strided call)")
     ap.add_argument("--graph", action="store_true",
@@ -158,15 +161,19 @@ def workload(name: str, no_mask: bool):
 
 
 def chosen_workload(args):
+    if args.W != 3 and args.op == "fwd":
+        raise SystemExit("bench.py: the forward runs at W = 3 only")
     wl = workload(args.workload, args.no_mask)
     if args.seq_len:
         wl = wl.resized(S=args.seq_len)
+    if args.W != 3:
+        wl = wl.resized(W=args.W)
     return wl
 
 
 def describe(wl, layout="sbh") -> dict:
     mask = "none" if wl.mask[0] == "none" else "(" + ",".join(str(v) for v in wl.mask) + ")"
-    return {"workload": wl.name, "layout": layout, "S": wl.S, "B": wl.B, "H": wl.H, "W": wl.W, "io_dtype": wl.dtype,
+    return {"workload": wl.name + ("" if wl.W == 3 else f"_w{wl.W}"), "layout": layout, "S": wl.S, "B": wl.B, "H": wl.H, "W": wl.W, "io_dtype": wl.dtype,
             "x_gradY": list(wl.x), "weight": list(wl.w), "mask": mask, "seed": 0,
             "l2": f"inputs {wl.algorithmic_bytes() / 1e9:.1f} GB per step > 129 MB L2; no flush"}
 
@@ -180,6 +187,15 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_sha256() -> str:
+    """One hash over the sources that make up the main kernel and its plan."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profiled_traffic():
     """Per-launch DRAM bytes of the main kernel from the committed ncu summary,
     if it was taken on the kernel source as it is now; else None."""
@@ -190,9 +206,7 @@ def profiled_traffic():
                 if ":" in line:
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        with open(KERNEL_SRC, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        if kv.get("kernels_cu_sha256") != sha:
+        if kv.get("source_sha256") != source_sha256():
             return None
         return int(kv["dram_bytes_per_launch_full"])
     except (OSError, KeyError, ValueError):
@@ -260,7 +274,7 @@ def gpu_arm(args):
     mask = None if host["mask"] is None else host["mask"].to(dev)
     gx = torch.empty_like(gy)
     gw = torch.empty_like(w)
-    nbytes = m.mcc1d_bwd_workspace_size(wl.S, wl.B, wl.H, wl.W, code, mask is not None)
+    nbytes = m.mcc1d_bwd_workspace_size(wl.S, wl.B, wl.H, 3, code, mask is not None)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -273,10 +287,11 @@ def gpu_arm(args):
         def step(st=None):  # noqa: F811
             m.mcc1d_fwd(x, w, mask, y, st or stream, wl.S, wl.B, wl.H, wl.W, code)
 
-    if args.layout == "bsh":
-        # the same values held as [B,S,H] buffers and passed as strided views
-        gy_v = gy.transpose(0, 1).contiguous().transpose(0, 1)
-        x_v = x.transpose(0, 1).contiguous().transpose(0, 1)
+    if args.layout == "bsh" or wl.W != 3:
+        # bsh: the same values held as [B,S,H] buffers and passed as strided
+        # views; other widths: the strided call with dense strides
+        gy_v = gy.transpose(0, 1).contiguous().transpose(0, 1) if args.layout == "bsh" else gy
+        x_v = x.transpose(0, 1).contiguous().transpose(0, 1) if args.layout == "bsh" else x
         desc = m.tensors(gy_v, x_v, w, mask, gx, gw)
         nbytes = m.mcc1d_bwd_ex_workspace_size(desc, wl.S, wl.B, wl.H, wl.W, code)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -330,7 +345,7 @@ def gpu_arm(args):
 
     # end to end: pinned host inputs -> device -> call -> host outputs, every step
     e2e = None
-    if not args.no_e2e and args.layout == "sbh" and args.op == "bwd":
+    if not args.no_e2e and args.layout == "sbh" and args.op == "bwd" and wl.W == 3:
         # Same call with every tensor in page-locked host memory: the kernel
         # reads gradY, x, weight and the mask over the host link and writes
         # gradX and gradWeight back, each step.

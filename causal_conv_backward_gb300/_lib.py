@@ -222,9 +222,9 @@ def mcc1d_version() -> int:
 
 def backward(gradY, x, weight, mask=None, *, gradX=None, gradWeight=None, workspace=None,
              stream=None):
-    """Convenience call on torch CUDA tensors: gradY, x [S,B,H], weight [3,H]
-    (bf16 or fp16), mask [B,S] bool/uint8 or None; inputs may be strided
-    views. Allocates whatever output or workspace is not given (with torch)
+    """Convenience call on torch CUDA tensors: gradY, x [S,B,H], weight [W,H]
+    (bf16 or fp16; W = 3 on the dense call, 1..8 through the strided one),
+    mask [B,S] bool/uint8 or None; inputs may be strided views. Allocates whatever output or workspace is not given (with torch)
     and returns (gradX, gradWeight)."""
     import torch
 
@@ -242,7 +242,8 @@ def backward(gradY, x, weight, mask=None, *, gradX=None, gradWeight=None, worksp
         gradWeight = torch.empty((W, H), dtype=weight.dtype, device=weight.device)
     if stream is None:
         stream = torch.cuda.current_stream(gradY.device)
-    dense = all(t.is_contiguous() for t in (gradY, x, weight)) and (mask is None or mask.is_contiguous())
+    dense = (W == 3 and all(t.is_contiguous() for t in (gradY, x, weight))
+             and (mask is None or mask.is_contiguous()))
     if dense:
         nbytes = mcc1d_bwd_workspace_size(S, B, H, W, code, mask is not None)
     else:

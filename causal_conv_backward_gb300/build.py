@@ -62,6 +62,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
         return r.stdout + r.stderr
 
+    # biggest translation units first, so they start early
+    order = sorted(range(len(cmds)), key=lambda k: -os.path.getsize(sources()[k]))
+    cmds = [cmds[k] for k in order]
+    objs = [objs[k] for k in order]
     with cf.ThreadPoolExecutor(max_workers=len(cmds)) as ex:
         logs = list(ex.map(run, cmds))
     if verbose:

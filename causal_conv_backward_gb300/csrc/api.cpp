@@ -123,7 +123,7 @@ int32_t make_ex(const mcc1d_tensors *t, int64_t S, int64_t B, int64_t H, int64_t
 {
     if (!t || !t->gradY || !t->x || !t->weight || !t->gradX || !t->gradWeight)
         return kErrNull;
-    const int32_t st = make_plan(S, B, H, W, dtype, &e->plan);
+    const int32_t st = make_plan_general(S, B, H, W, dtype, &e->plan);
     if (st != kOk)
         return st;
     Layout in;
@@ -220,7 +220,10 @@ extern "C" int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *m
     if (!x || !weight || !y)
         return kErrNull;
     Plan p;
-    const int32_t st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, &p);
+    int32_t st = validate_shape(S, B, H, W, dtype);
+    if (st != kOk)
+        return st;
+    st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, &p);
     if (st != kOk)
         return st;
     if (!aligned16(x) || !aligned16(weight) || !aligned16(y))

@@ -17,6 +17,16 @@ int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype
         return kErrInvalid;
     if (W != kW)
         return kErrShape;
+    return validate_shape_w(S, B, H, W, dtype);
+}
+
+// The same limits with any kernel width 1 <= W <= kMaxW.
+int32_t validate_shape_w(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype)
+{
+    if (dtype != 0 && dtype != 1)
+        return kErrInvalid;
+    if (W < 1 || W > kMaxW)
+        return kErrShape;
     if (B < 1 || B > 32 || S < 1 || S > 524288 || B * S > 524288)
         return kErrShape;
     if (H < 384 || H > 24576 || H % 64 != 0)
@@ -26,6 +36,18 @@ int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype
 
 int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p)
 {
+    const int32_t st = validate_shape(S, B, H, W, dtype);
+    if (st != kOk)
+        return st;
+    return make_plan_general(S, B, H, W, dtype, p);
+}
+
+int32_t make_plan_general(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p)
+{
+    // Wide kernels keep W accumulators per channel: 4 channels per thread
+    // and 1024-channel blocks keep them in registers.
+    if (W >= 4)
+        return make_plan_for(S, B, H, W, dtype, 8, kHbWidthNarrow, p);
     const int32_t st = make_plan_for(S, B, H, W, dtype, 8, kHbWidthWide, p);
     if (st != kOk || p->rows_total / p->ncta >= kWideMinRowsPerCta)
         return st;
@@ -35,13 +57,14 @@ int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Pla
 int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
                       int target_consumer_warps, int max_hb_width, Plan *p)
 {
-    int32_t st = validate_shape(S, B, H, W, dtype);
+    int32_t st = validate_shape_w(S, B, H, W, dtype);
     if (st != kOk)
         return st;
     memset(p, 0, sizeof(*p));
     p->S = S;
     p->B = B;
     p->H = H;
+    p->W = (int32_t)W;
     p->dtype = dtype;
 
     // H-blocks: as few as possible of at most max_hb_width halves, balanced,
@@ -54,6 +77,8 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     p->vec = 8;
     if ((p->hb_width / 8) % 32 != 0 && (p->hb_width / 4) % 32 == 0 && p->hb_width / 4 <= 128)
         p->vec = 4;
+    if (W >= 4)
+        p->vec = 4;
     const int vectors = p->hb_width / p->vec;
     p->consumer_warps = (int32_t)ceil_div(vectors, 32);
     p->threads = 32 * (p->consumer_warps + 1);
@@ -65,18 +90,21 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     p->ctas_per_sm = cps;
 
     p->row_bytes = (uint32_t)p->hb_width * 2u;
-    const uint32_t outer_bytes = (uint32_t)p->consumer_warps * 32u * 3u * (uint32_t)p->vec * 4u;
+    const uint32_t outer_bytes = (uint32_t)p->consumer_warps * 32u * (uint32_t)W * (uint32_t)p->vec * 4u;
     const int64_t budget = kSmemPerSM / cps - kSmemReservedPerCta;
 
     // Rows per stage and ring depth: the deepest R (fewer barrier round trips)
-    // that still leaves a ring of three slots, else R = 4 with what fits.
-    const int r_choices[3] = {8, 6, 4};
+    // that still leaves a ring of three slots, else the last choice with what
+    // fits. Widths other than 3 have one instance, R = 6.
+    const int r_w3[3] = {8, 6, 4}, r_other[1] = {6};
+    const int *r_choices = W == 3 ? r_w3 : r_other;
+    const int n_choices = W == 3 ? 3 : 1;
     p->rows_per_stage = 0;
-    for (int t = 0; t < 3; ++t) {
+    for (int t = 0; t < n_choices; ++t) {
         const int R = r_choices[t];
-        const int64_t slot = (int64_t)(2 * R + 2) * p->row_bytes;
+        const int64_t slot = (int64_t)(2 * R + W - 1) * p->row_bytes;
         int64_t ns = (budget - outer_bytes - 64) / (slot + 48);
-        if (ns >= 3 || t == 2) {
+        if (ns >= 3 || t == n_choices - 1) {
             if (ns > 6)
                 ns = 6;
             if (ns < 2)
@@ -127,8 +155,8 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
 
     p->ws_status_off = kHeaderBytes;
     p->ws_part_off = kHeaderBytes + (uint64_t)round_up(4 * ncta, 256);
-    p->ws_bytes = p->ws_part_off + (uint64_t)p->nslots * kW * (uint64_t)p->hb_width * 4u;
-    p->reduce_blocks = (int32_t)(p->n_hb * kW * ceil_div(p->hb_width, kReduceCols));
+    p->ws_bytes = p->ws_part_off + (uint64_t)p->nslots * (uint64_t)W * (uint64_t)p->hb_width * 4u;
+    p->reduce_blocks = (int32_t)(p->n_hb * W * ceil_div(p->hb_width, kReduceCols));
     return kOk;
 }
 

@@ -15,7 +15,8 @@
 
 namespace mcc1d {
 
-constexpr int kW = 3;                 // the only kernel width the operator supports
+constexpr int kW = 3;                 // the only kernel width the operator page supports
+constexpr int kMaxW = 8;              // widest kernel the strided entry points accept
 constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs
 constexpr int kSmemPerSM = 233472;    // 228 KB of shared memory per SM
 constexpr int kSmemPerCtaMax = 232448;// 227 KB opt-in maximum per CTA
@@ -44,6 +45,7 @@ enum : int32_t {
 
 struct Plan {
     int64_t S, B, H;
+    int32_t W;               // kernel width (taps)
     int32_t dtype;           // 0 bf16, 1 fp16
     // H is cut into n_hb blocks of hb_width halves (the last may be narrower).
     int32_t hb_width, n_hb;
@@ -52,7 +54,7 @@ struct Plan {
     // or 4: an 8-byte vector) of the H-block.
     int32_t vec;
     int32_t consumer_warps, threads;
-    int32_t rows_per_stage;  // R: rows of x (and R+2 of gradY) per ring slot
+    int32_t rows_per_stage;  // R: rows of x (and R+W-1 of gradY) per ring slot
     int32_t stages;          // ring slots
     int32_t ctas_per_sm;
     // Work: the rows (hb, j, i), flattened with i fastest, N = n_hb*B*S, are
@@ -66,10 +68,10 @@ struct Plan {
     int32_t nslots;
     // Shared memory layout (bytes from the dynamic smem base).
     uint32_t row_bytes;      // stride of one staged row = hb_width * 2
-    uint32_t slot_bytes;     // (2R + 2) rows
+    uint32_t slot_bytes;     // (2R + W - 1) rows
     uint32_t off_mask;       // stages x 32 mask bytes
     uint32_t off_bar;        // 2 x stages mbarriers
-    uint32_t off_outer;      // 3 * vec fp32 accumulators per consumer thread
+    uint32_t off_outer;      // W * vec fp32 accumulators per consumer thread
     uint32_t smem_bytes;
     // Workspace layout: header | per-CTA status words | fp32 partials
     // [nslots][W][hb_width].
@@ -98,9 +100,10 @@ inline Layout dense_layout(int64_t S, int64_t B, int64_t H)
     return L;
 }
 
-// Shape and dtype checks of the page's constraints. Returns kOk, kErrInvalid
-// (dtype) or kErrShape.
+// Shape and dtype checks of the page's constraints (W == 3). Returns kOk,
+// kErrInvalid (dtype) or kErrShape. validate_shape_w allows 1 <= W <= kMaxW.
 int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype);
+int32_t validate_shape_w(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype);
 
 // Fills *p for a valid shape; returns the validate_shape status otherwise.
 // make_plan is the backward's plan: 8 consumer warps per SM (its register
@@ -108,6 +111,8 @@ int32_t validate_shape(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype
 // larger copies to pay, else 2 KB. make_plan_for fixes both choices (the
 // forward, at about 96 registers a thread, asks for more warps).
 int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p);
+// The backward's plan for any width 1 <= W <= kMaxW (the strided entry points).
+int32_t make_plan_general(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p);
 int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
                       int target_consumer_warps, int max_hb_width, Plan *p);
 

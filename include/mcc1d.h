@@ -182,7 +182,10 @@ typedef struct mcc1d_tensors {
  * Phase 1 for strided tensors (page: the same GetWorkspaceSize call, which
  * receives the tensors themselves). The workspace size depends on the
  * layouts and base pointers of gradY and x. Validation as
- * mcc1d_bwd_workspace_size, plus: MCC1D_ERR_PARAM_NULLPTR for a null
+ * mcc1d_bwd_workspace_size except for the kernel width: the strided calls
+ * take any 1 <= W <= 8 (the page supports W = 3 only today, 约束说明 /
+ * constraints; its formulas, 计算公式, are written for any W: gradX sums W
+ * taps and gradWeight has W rows). Plus: MCC1D_ERR_PARAM_NULLPTR for a null
  * descriptor or required pointer; MCC1D_ERR_PARAM_INVALID for a negative
  * stride, a 16-bit input pointer that is not 2-byte aligned, or an output
  * pointer that is not 16-byte aligned.

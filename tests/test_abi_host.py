@@ -177,3 +177,17 @@ def test_fwd_rejects_before_any_launch(lib):
     assert call(x=0x1008) == INVALID and call(y=0x3002) == INVALID
     assert call(dt=2) == INVALID
     assert call(B=0) == SHAPE and call(H=4000) == SHAPE and call(W=5) == SHAPE
+
+
+def test_ex_accepts_widths_one_to_eight(lib):
+    """The strided calls take any kernel width 1..8 (the page's calls keep W = 3)."""
+    sizes = []
+    for W in range(1, 9):
+        t = desc(ws_=[384, 1])
+        st, n = ex_size(t, W=W)
+        assert st == 0, W
+        sizes.append(n)
+    assert sizes == sorted(sizes)  # W partial rows per slot
+    assert ex_size(desc(), W=0)[0] == SHAPE
+    assert ex_size(desc(), W=9)[0] == SHAPE
+    assert ws(64, 2, 384, W=4)[0] == SHAPE   # page call: W must be 3
