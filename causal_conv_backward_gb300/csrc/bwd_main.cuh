@@ -165,6 +165,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
     constexpr int CH = 2 * NP;                                     // channels per thread
     constexpr int WH = W - 1;                                      // rows of the window
+    constexpr bool kStageSums = W <= 3;                            // per-stage gradWeight level
     float *outer = reinterpret_cast<float *>(smem + p.off_outer);  // [W*CH][nct]
     const int64_t row_stride = 2 * (int64_t)p.B * p.H;             // bytes from row i to i+1
     const int c = blockIdx.x;
@@ -257,12 +258,18 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                     win[q] = load_masked<DT, NP>(gys + (size_t)q * p.row_bytes, ms[q]);
             }
             uint8_t *gxp = p.gx + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
+            // gradWeight of this stage: W <= 3 sums the stage's R rows on
+            // their own before adding them to the 16-stage level; wider
+            // kernels add each row straight into that level, which frees
+            // W*CH registers per thread (the sums keep the same three levels
+            // otherwise: rows, 16-stage blocks, the whole CTA range).
             float2 in[W][NP];
 #pragma unroll
             for (int k = 0; k < W; ++k)
 #pragma unroll
                 for (int e = 0; e < NP; ++e)
                     in[k][e] = make_float2(0.f, 0.f);
+            float2 (&acc)[W][NP] = kStageSums ? in : mid;
             // One row i+r: gradX from the window gYm(i+r .. i+r+W-2) and the
             // staged gradY row i+r+W-1; the W gradWeight taps against x(i+r).
             auto row = [&](int r) {
@@ -298,7 +305,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                     // gradWeight tap k pairs x(i) with gYm(i+W-1-k)
 #pragma unroll
                     for (int k = 0; k < W; ++k)
-                        in[W - 1 - k][e] = fma2(k < WH ? win[k].e[e] : gn.e[e], xv.e[e], in[W - 1 - k][e]);
+                        acc[W - 1 - k][e] = fma2(k < WH ? win[k].e[e] : gn.e[e], xv.e[e], acc[W - 1 - k][e]);
                 }
                 store_cs<NP>(gxp + (int64_t)r * row_stride, o);
 #pragma unroll
@@ -319,11 +326,13 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                     if (r < n)
                         row(r);
             }
+            if constexpr (kStageSums) {
 #pragma unroll
-            for (int k = 0; k < W; ++k)
+                for (int k = 0; k < W; ++k)
 #pragma unroll
-                for (int e = 0; e < NP; ++e)
-                    mid[k][e] = add2(mid[k][e], in[k][e]);
+                    for (int e = 0; e < NP; ++e)
+                        mid[k][e] = add2(mid[k][e], in[k][e]);
+            }
             if (++since_flush == kFlushStages) {
 #pragma unroll
                 for (int k = 0; k < W; ++k)
@@ -353,7 +362,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 
 // ------------------------------------------------------------------ kernels
 template <int DT, int R, int NP, int W>
-__global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_constant__ MainParams p)
+__device__ __forceinline__ void main_body(const MainParams &p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_err;
@@ -390,6 +399,20 @@ __global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_const
     __threadfence();
     __syncthreads();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <int DT, int R, int NP, int W>
+__global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_constant__ MainParams p)
+{
+    main_body<DT, R, NP, W>(p);
+}
+
+// The same kernel held to the registers that let two CTAs share an SM
+// (65536 / (2 * 288) per thread), for the plans that run two per SM.
+template <int DT, int R, int NP, int W>
+__global__ void __launch_bounds__(kMaxThreads, 2) mcc1d_bwd_main_x2(const __grid_constant__ MainParams p)
+{
+    main_body<DT, R, NP, W>(p);
 }
 
 typedef void (*MainFn)(MainParams);

@@ -1,7 +1,8 @@
 // kernels_w.cu - instances of the backward's main kernel for widths W other
 // than 3 (one rows-per-stage choice, R = 6), for the strided entry points,
 // which accept 1 <= W <= 8. Widths from 4 up keep 4 channels per thread so
-// their W accumulators per channel stay in registers. Compiled apart from
+// their W accumulators per channel stay in registers; widths 4 and 5 run two
+// CTAs per SM under the matching register bound. Compiled apart from
 // kernels.cu so the two build in parallel.
 #include "bwd_main.cuh"
 
@@ -10,7 +11,9 @@ namespace mcc1d {
 template <int DT, int W>
 static MainFn pick(int vec)
 {
-    if constexpr (W >= 4)
+    if constexpr (W >= 4 && W <= kTwoCtaMaxW)
+        return vec == 4 ? mcc1d_bwd_main_x2<DT, 6, 2, W> : nullptr;
+    else if constexpr (W >= 4)
         return vec == 4 ? mcc1d_bwd_main<DT, 6, 2, W> : nullptr;
     else
         return vec == 4 ? mcc1d_bwd_main<DT, 6, 2, W> : mcc1d_bwd_main<DT, 6, 4, W>;

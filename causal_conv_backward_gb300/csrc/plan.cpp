@@ -45,9 +45,11 @@ int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Pla
 int32_t make_plan_general(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p)
 {
     // Wide kernels keep W accumulators per channel: 4 channels per thread
-    // and 1024-channel blocks keep them in registers.
+    // and 1024-channel blocks keep them in registers. Up to kTwoCtaMaxW they
+    // fit the two-CTA register bound, and sixteen consumer warps per SM hide
+    // the longer arithmetic of each row.
     if (W >= 4)
-        return make_plan_for(S, B, H, W, dtype, 8, kHbWidthNarrow, p);
+        return make_plan_for(S, B, H, W, dtype, W <= kTwoCtaMaxW ? 16 : 8, kHbWidthNarrow, p);
     const int32_t st = make_plan_for(S, B, H, W, dtype, 8, kHbWidthWide, p);
     if (st != kOk || p->rows_total / p->ncta >= kWideMinRowsPerCta)
         return st;

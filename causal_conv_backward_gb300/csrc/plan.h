@@ -17,6 +17,7 @@ namespace mcc1d {
 
 constexpr int kW = 3;                 // the only kernel width the operator page supports
 constexpr int kMaxW = 8;              // widest kernel the strided entry points accept
+constexpr int kTwoCtaMaxW = 5;        // widths 4 .. kTwoCtaMaxW run two CTAs per SM
 constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs
 constexpr int kSmemPerSM = 233472;    // 228 KB of shared memory per SM
 constexpr int kSmemPerCtaMax = 232448;// 227 KB opt-in maximum per CTA
