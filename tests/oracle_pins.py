@@ -231,10 +231,11 @@ def pin_jacobian_bruteforce(orc):
     """gradX = J_x^T gradY and gradWeight = J_w^T gradY, with J built column by
     column from the forward evaluated on unit inputs (the forward is linear in
     x for fixed w and in w for fixed x). Small dyadic values keep every sum
-    exact, so the comparison is exact. Covers W = 1..4."""
+    exact, so the comparison is exact. Covers every width the strided calls
+    accept, W = 1..8 (widths above S included)."""
     rng = np.random.default_rng(17)
     for dt in ("bf16", "fp16"):
-        for W in (1, 2, 3, 4):
+        for W in range(1, 9):
             for S in (1, 2, 3, 4, 5, 6):
                 for B in (1, 2):
                     H = 2
@@ -302,7 +303,9 @@ def pin_torch_autograd(orc):
     values rounded once."""
     rng = np.random.default_rng(29)
     for dt in ("bf16", "fp16"):
-        for (S, B, H, W) in ((1, 2, 5, 3), (5, 1, 3, 3), (33, 3, 7, 3), (64, 2, 384, 3), (9, 2, 4, 2), (9, 2, 4, 5)):
+        for (S, B, H, W) in ((1, 2, 5, 3), (5, 1, 3, 3), (33, 3, 7, 3), (64, 2, 384, 3), (9, 2, 4, 2),
+                             (9, 2, 4, 5), (17, 2, 6, 1), (17, 2, 6, 4), (17, 2, 6, 6), (17, 2, 6, 8),
+                             (3, 2, 4, 8)):
             gy, x, w = (rand_bits(rng, (S, B, H), dt), rand_bits(rng, (S, B, H), dt),
                         rand_bits(rng, (W, H), dt))
             mask = (rng.random((B, S)) < 0.8).astype(np.uint8)
