@@ -62,6 +62,9 @@ def parse_args(argv=None):
                     help="kernel width; other than 3 runs through the strided call mcc1d_bwd_ex")
     ap.add_argument("--layout", choices=["sbh", "bsh"], default="sbh",
                     help="bsh: gradY and x live as [B,S,H] buffers seen as [S,B,H] (strided call)")
+    ap.add_argument("--l2", choices=["auto", "flush", "hot"], default="auto",
+                    help="flush: write a 2x-L2 buffer between timed calls (timed per call, flush "
+                         "excluded); hot: no flush; auto: flush when one call moves < 4x L2")
     ap.add_argument("--graph", action="store_true",
                     help="capture the K timed calls in one CUDA graph (removes host launch gaps)")
     ap.add_argument("--seq-len", type=int, default=0,
@@ -171,11 +174,24 @@ def chosen_workload(args):
     return wl
 
 
-def describe(wl, layout="sbh") -> dict:
+L2_BYTES = 129 * 1024 * 1024
+
+
+def l2_mode(args, alg_bytes: int) -> str:
+    if args.l2 != "auto":
+        return args.l2
+    return "flush" if alg_bytes < 4 * L2_BYTES else "hot"
+
+
+def describe(wl, layout="sbh", l2="hot", alg_bytes=None) -> dict:
     mask = "none" if wl.mask[0] == "none" else "(" + ",".join(str(v) for v in wl.mask) + ")"
     return {"workload": wl.name + ("" if wl.W == 3 else f"_w{wl.W}"), "layout": layout, "S": wl.S, "B": wl.B, "H": wl.H, "W": wl.W, "io_dtype": wl.dtype,
             "x_gradY": list(wl.x), "weight": list(wl.w), "mask": mask, "seed": 0,
-            "l2": f"inputs {wl.algorithmic_bytes() / 1e9:.1f} GB per step > 129 MB L2; no flush"}
+            "l2": (f"flushed: a {2 * L2_BYTES >> 20} MiB buffer written between timed calls (not timed)"
+                   if l2 == "flush" else
+                   f"hot: {(alg_bytes or wl.algorithmic_bytes()) / 1e9:.3f} GB per call"
+                   + (" > 129 MB L2; no flush" if (alg_bytes or wl.algorithmic_bytes()) > L2_BYTES
+                      else ", fits in the 129 MB L2; no flush (hot-cache number)"))}
 
 
 def measured_peak():
@@ -308,6 +324,11 @@ def gpu_arm(args):
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     sampler = ClockSampler(f"GPU-{gpu_id}" if gpu_id is not None else str(local))
     K = args.steps
+    alg = wl.algorithmic_bytes() if args.op == "bwd" else wl.fwd_algorithmic_bytes()
+    l2 = l2_mode(args, alg)
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if l2 == "flush" else None
+    if flush_buf is not None and args.graph:
+        raise SystemExit("bench.py: --graph times K calls back to back; it cannot flush L2 between them")
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     graph = None
@@ -328,6 +349,8 @@ def gpu_arm(args):
         graph.replay()
     else:
         for k in range(K):
+            if flush_buf is not None:
+                flush_buf.fill_(k & 255)   # evict the previous call's lines from L2
             ev[k][0].record(stream)
             step()
             ev[k][1].record(stream)
@@ -338,7 +361,8 @@ def gpu_arm(args):
     elapsed = start.elapsed_time(end) / 1e3
     per_call = ([elapsed / K] * K if graph is not None
                 else [a.elapsed_time(b) / 1e3 for a, b in ev])
-    alg = wl.algorithmic_bytes() if args.op == "bwd" else wl.fwd_algorithmic_bytes()
+    if flush_buf is not None:
+        elapsed = sum(per_call)   # the calls alone, without the flushes between them
     t_max, bytes_all = aggregate(dist, elapsed, float(alg) * K, dev)
     value = bytes_all / t_max / 1e9
     tokens_h = float(wl.E) * K * world / t_max
@@ -380,7 +404,11 @@ def gpu_arm(args):
     avg_call = sum(per_call) / len(per_call)
     achieved = alg / avg_call / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                "frac": round(achieved / peak, 4),
+                # the committed ncu record covers the backward's main kernel on the
+                # bench workload (W = 3, dense [S,B,H]) only
+                "traffic": (profiled_traffic() if (args.op == "bwd" and wl.W == 3 and args.layout == "sbh"
+                                                   and wl == workload(WORKLOAD, False)) else None),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "kernel": ("mcc1d_bwd_main (timed as the whole call: main + reduce)" if args.op == "bwd"
@@ -401,8 +429,8 @@ def gpu_arm(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(t_max / K * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded generator; fp16 bit patterns)",
-            "config": describe(wl, args.layout), "tokens_h_per_s": float(f"{tokens_h:.4e}"),
+            "data": f"synthetic (seeded generator; {wl.dtype} bit patterns)",
+            "config": describe(wl, args.layout, l2, alg), "tokens_h_per_s": float(f"{tokens_h:.4e}"),
             "frac_of_peak": round(value / world / peak, 4),
             "op": args.op,
             "e2e": e2e, "gpu_launches": (2 if args.op == "bwd" else 1) * K, "roofline": roofline,
@@ -427,7 +455,7 @@ def reference_arm(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded generator; fp16 bit patterns)", "config": describe(wl),
+        "data": f"synthetic (seeded generator; {wl.dtype} bit patterns)", "config": describe(wl),
         "tokens_h_per_s": float(f"{sample.E / t:.4e}"),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nt, "kind": "oracle",
                          "sample": f"per step: first {sample.S} of {wl.S} positions of all "
