@@ -24,10 +24,10 @@ constexpr int kMaxThreads = 288;                  // 8 consumer warps + producer
 struct MainParams {
     const uint8_t *gy;     // [S,B,H] 16-bit elements, addressed in bytes
     const uint8_t *x;      // [S,B,H]
-    const uint16_t *w;     // [3,H]
+    const uint16_t *w;     // [W,H]
     const uint8_t *mask;   // [B,S] or null
     uint8_t *gx;           // [S,B,H]
-    float *part;           // [nslots][3][hb_width]
+    float *part;           // [nslots][W][hb_width]
     int32_t *status;       // [ncta]
     int64_t S, BS, H, N;
     int32_t B, hb_width, ncta, stages;

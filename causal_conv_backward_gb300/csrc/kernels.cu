@@ -1,10 +1,11 @@
 // kernels.cu - sm_103a kernels of the masked causal depthwise conv1d backward.
 //
 // Operation (CANN operator page "aclnnMaskedCausalConv1dBackward", 功能说明 /
-// 计算公式), for every depthwise channel h:
+// 计算公式), for every depthwise channel h and kernel width W (3 on the page):
 //   gYm(i,j)      = mask(j,i) * gradY(i,j)
-//   gradX(i,j)    = gYm(i,j)*w(2) + gYm(i+1,j)*w(1) + gYm(i+2,j)*w(0)
-//   gradWeight(k) = sum_{j,i} gYm(i+2-k,j) * x(i,j)
+//   gradX(i,j)    = sum_{k<W} gYm(i+k,j) * w(W-1-k)
+//                   (W = 3: gYm(i)*w(2) + gYm(i+1)*w(1) + gYm(i+2)*w(0))
+//   gradWeight(k) = sum_{j,i} gYm(i+W-1-k,j) * x(i,j)
 // with gYm zero for i >= S.
 //
 // The work is pure streaming: each element of gradY and x is read once and
@@ -15,16 +16,17 @@
 //   The rows (hb, j, i) - H-block, batch, sequence position, i fastest - are
 //   split into ncta contiguous ranges. Warp 0 is the producer: it walks its
 //   CTA's range in stages of R rows and, per stage, copies the R rows of x and
-//   the R rows of gradY two positions ahead (plus the first two rows when a
+//   the R rows of gradY W-1 positions ahead (plus the first W-1 rows when a
 //   sequence starts) into a ring slot with cp.async.bulk, completing on the
 //   slot's "full" mbarrier; it also stores the stage's mask bytes in the slot.
 //   The consumer warps own one 16-byte vector (8 channels) each (8 bytes,
 //   4 channels, when that fills the warps better, as for H = 384), keep the last
-//   two masked gradY rows in registers, and per row form gradX with a
-//   compensated three-term sum (exact fp32 products + TwoSum), store it with
-//   a streaming 16-byte store, and accumulate the three gradWeight taps in
-//   fp32. Each CTA writes one fp32 partial [3][H-block] per H-block it
-//   touched into the workspace.
+//   W-1 masked gradY rows in registers, and per row form gradX with a
+//   compensated W-term sum (exact fp32 products + TwoSum), store it with
+//   a streaming 16-byte store, and accumulate the W gradWeight taps in
+//   fp32. Each CTA writes one fp32 partial [W][H-block] per H-block it
+//   touched into the workspace. The main kernel's templates live in
+//   bwd_main.cuh; this file instantiates W = 3, kernels_w.cu the other widths.
 // mcc1d_bwd_reduce (programmatic dependent launch):
 //   Sums the partials of every gradWeight column in a fixed order (64 serial
 //   slices over the CTAs, then a pairwise tree), rounds once to the 16-bit
@@ -51,7 +53,7 @@ struct ReduceParams {
     const float *part;
     const int32_t *status;
     int32_t *header;
-    uint8_t *gw;           // [3,H]
+    uint8_t *gw;           // [W,H]
     int64_t H;
     int32_t hb_width, ncta, nchunk, W;
     int32_t c_lo[kMaxHb], c_hi[kMaxHb], slot_base[kMaxHb];
