@@ -364,6 +364,9 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 template <int DT, int R, int NP, int W>
 __device__ __forceinline__ void main_body(const MainParams &p)
 {
+    // one producer lane per staged row (R + W - 1 gradY rows, R x rows), and
+    // the stage's mask bytes fit the slot's 32-byte mask record
+    static_assert(2 * R + W - 1 <= 32, "a stage must not stage more rows than a warp has lanes");
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_err;
     const int c = blockIdx.x;

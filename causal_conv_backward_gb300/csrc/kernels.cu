@@ -153,6 +153,11 @@ static MainFn main_for(int R)
     case 4: return mcc1d_bwd_main<DT, 4, NP, 3>;
     case 6: return mcc1d_bwd_main<DT, 6, NP, 3>;
     case 8: return mcc1d_bwd_main<DT, 8, NP, 3>;
+    case 14:  // deep stages of narrow rows (4 channels per thread) only
+        if constexpr (NP == 2)
+            return mcc1d_bwd_main<DT, 14, NP, 3>;
+        else
+            return nullptr;
     default: return nullptr;
     }
 }

@@ -89,6 +89,17 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     int cps = (int)ceil_div(target_consumer_warps, p->consumer_warps);
     while (cps > 1 && cps * p->threads > 2048)
         --cps;
+    // ... and no more CTAs than the register file holds: each of an SM's four
+    // schedulers has 16384 registers, so at r registers per thread it keeps
+    // 16384 / (32 r) warps. r is the bound the kernel is compiled under (96 for
+    // the two-CTA kernels, 168 for the others), so a plan never asks for CTAs
+    // that would wait for a second wave.
+    {
+        const int regs = (W >= 4 && W <= kTwoCtaMaxW) ? kRegsTwoCta : kRegsOneCta;
+        const int warps_per_sm = 4 * (16384 / (32 * regs));
+        while (cps > 1 && cps * (p->threads / 32) > warps_per_sm)
+            --cps;
+    }
     p->ctas_per_sm = cps;
 
     p->row_bytes = (uint32_t)p->hb_width * 2u;
@@ -97,10 +108,19 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
 
     // Rows per stage and ring depth: the deepest R (fewer barrier round trips)
     // that still leaves a ring of three slots, else the last choice with what
-    // fits. Widths other than 3 have one instance, R = 6.
-    const int r_w3[3] = {8, 6, 4}, r_other[1] = {6};
-    const int *r_choices = W == 3 ? r_w3 : r_other;
-    const int n_choices = W == 3 ? 3 : 1;
+    // fits. Widths other than 3 have one instance, R = 6. Narrow rows (4
+    // channels per thread) that are copied one row at a time (B > 1 or several
+    // H-blocks) spend most of the producer's time per stage, not per byte, so
+    // long CTA ranges take R = 14 there (2R + W - 1 = 30 copies, one per lane).
+    int64_t ncta_est = (int64_t)kNumSMs * cps;
+    const int64_t rows_all = (int64_t)p->n_hb * B * S;
+    if (ncta_est > ceil_div(rows_all, kMinRowsPerCta))
+        ncta_est = ceil_div(rows_all, kMinRowsPerCta);
+    const bool row_copies = !(B == 1 && p->n_hb == 1);
+    const bool deep = W == 3 && p->vec == 4 && row_copies && rows_all / ncta_est >= kDeepMinRowsPerCta;
+    const int r_w3[3] = {8, 6, 4}, r_deep[4] = {14, 8, 6, 4}, r_other[1] = {6};
+    const int *r_choices = deep ? r_deep : W == 3 ? r_w3 : r_other;
+    const int n_choices = deep ? 4 : W == 3 ? 3 : 1;
     p->rows_per_stage = 0;
     for (int t = 0; t < n_choices; ++t) {
         const int R = r_choices[t];

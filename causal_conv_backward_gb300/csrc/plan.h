@@ -18,6 +18,9 @@ namespace mcc1d {
 constexpr int kW = 3;                 // the only kernel width the operator page supports
 constexpr int kMaxW = 8;              // widest kernel the strided entry points accept
 constexpr int kTwoCtaMaxW = 5;        // widths 4 .. kTwoCtaMaxW run two CTAs per SM
+constexpr int kRegsOneCta = 168;      // register bound of the main kernel (288 threads, one CTA)
+constexpr int kRegsTwoCta = 96;       // ... and of its two-CTA form (mcc1d_bwd_main_x2)
+constexpr int kDeepMinRowsPerCta = 256;  // CTA range long enough for 14-row stages
 constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs
 constexpr int kSmemPerSM = 233472;    // 228 KB of shared memory per SM
 constexpr int kSmemPerCtaMax = 232448;// 227 KB opt-in maximum per CTA

@@ -87,6 +87,21 @@ def test_edge_shapes(S, B, H, dt):
     check_against_oracle(wl, inp, gx, gw, status)
 
 
+# Narrow rows (H = 384, 4 channels per thread) copied one row at a time (B > 1)
+# over long CTA ranges take 14-row stages; these shapes reach that plan, with
+# sequence and CTA-range ends that fall mid-stage.
+DEEP = [(65536, 2, 384, "bf16", ("bernoulli", 0.9)), (16384, 8, 384, "fp16", ("prefix",)),
+        (40001, 3, 384, "bf16", ("spans", 0.2, 64, 1024)), (9001, 13, 384, "fp16", ("none",))]
+
+
+@pytest.mark.parametrize("S,B,H,dt,mask", DEEP, ids=[f"s{a}_b{b}_h{c}_{d}_{e[0]}" for a, b, c, d, e in DEEP])
+def test_narrow_deep_stages(S, B, H, dt, mask):
+    wl = datagen.Workload("deep", S, B, H, dt, mask=mask)
+    inp = datagen.generate(wl, seed=S)
+    gx, gw, status, _ = run_cuda(inp, S, B, H, dt)
+    check_against_oracle(wl, inp, gx, gw, status)
+
+
 def test_page_sample_zeros():
     """The operator page's call example: S=1, B=2, H=384, fp16, every input
     zero and a mask of zero bytes: both outputs are zero."""
