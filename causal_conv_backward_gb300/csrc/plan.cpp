@@ -49,15 +49,16 @@ int32_t make_plan_general(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dt
     // fit the two-CTA register bound, and sixteen consumer warps per SM hide
     // the longer arithmetic of each row.
     if (W >= 4)
-        return make_plan_for(S, B, H, W, dtype, W <= kTwoCtaMaxW ? 16 : 8, kHbWidthNarrow, p);
-    const int32_t st = make_plan_for(S, B, H, W, dtype, 8, kHbWidthWide, p);
+        return make_plan_for(S, B, H, W, dtype, W <= kTwoCtaMaxW ? 16 : 8, kHbWidthNarrow,
+                             bwd_regs_bound(W), p);
+    const int32_t st = make_plan_for(S, B, H, W, dtype, 8, kHbWidthWide, bwd_regs_bound(W), p);
     if (st != kOk || p->rows_total / p->ncta >= kWideMinRowsPerCta)
         return st;
-    return make_plan_for(S, B, H, W, dtype, 8, kHbWidthNarrow, p);
+    return make_plan_for(S, B, H, W, dtype, 8, kHbWidthNarrow, bwd_regs_bound(W), p);
 }
 
 int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
-                      int target_consumer_warps, int max_hb_width, Plan *p)
+                      int target_consumer_warps, int max_hb_width, int regs_bound, Plan *p)
 {
     int32_t st = validate_shape_w(S, B, H, W, dtype);
     if (st != kOk)
@@ -91,12 +92,10 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
         --cps;
     // ... and no more CTAs than the register file holds: each of an SM's four
     // schedulers has 16384 registers, so at r registers per thread it keeps
-    // 16384 / (32 r) warps. r is the bound the kernel is compiled under (96 for
-    // the two-CTA kernels, 168 for the others), so a plan never asks for CTAs
-    // that would wait for a second wave.
-    {
-        const int regs = (W >= 4 && W <= kTwoCtaMaxW) ? kRegsTwoCta : kRegsOneCta;
-        const int warps_per_sm = 4 * (16384 / (32 * regs));
+    // 16384 / (32 r) warps. r is the bound the kernel is compiled under, so a
+    // plan never asks for CTAs that would wait for a second wave.
+    if (regs_bound > 0) {
+        const int warps_per_sm = 4 * (16384 / (32 * regs_bound));
         while (cps > 1 && cps * (p->threads / 32) > warps_per_sm)
             --cps;
     }
