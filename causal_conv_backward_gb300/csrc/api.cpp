@@ -223,12 +223,18 @@ extern "C" int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *m
     int32_t st = validate_shape(S, B, H, W, dtype);
     if (st != kOk)
         return st;
-    // No register cap: the forward (96 registers a thread at 8 channels, 69 at
-    // 4) fits its 16 consumer warps per SM, and its results do not depend on
-    // the CTA partition (no reduction).
+    // The forward's results do not depend on the CTA partition (no
+    // reduction), so its plan may use the compiled kernel's register count,
+    // asked of the runtime, to keep every CTA resident.
     st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, 0, &p);
     if (st != kOk)
         return st;
+    const int regs = fwd_kernel_regs(p.dtype, p.vec);
+    if (regs > 0) {
+        st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, regs, &p);
+        if (st != kOk)
+            return st;
+    }
     if (!aligned16(x) || !aligned16(weight) || !aligned16(y))
         return kErrInvalid;
     return launch_fwd(p, x, weight, mask_or_null, y, device_status_or_null,

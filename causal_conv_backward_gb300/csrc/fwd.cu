@@ -263,6 +263,26 @@ static FwdFn fwd_kernel(int dtype, int vec)
     return vec == 4 ? mcc1d_fwd_main<1, kFwdR, 2> : mcc1d_fwd_main<1, kFwdR, 4>;
 }
 
+int fwd_kernel_regs(int dtype, int vec)
+{
+    // registers per thread of the forward instance (cached per device and
+    // instance; 0 when the runtime cannot say)
+    static std::atomic<int> cache[64][4];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    const int slot = dtype * 2 + (vec == 4 ? 1 : 0);
+    std::atomic<int> &c = cache[dev & 63][slot];
+    int r = c.load(std::memory_order_acquire);
+    if (r > 0)
+        return r;
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, reinterpret_cast<const void *>(fwd_kernel(dtype, vec))) != cudaSuccess)
+        return 0;
+    c.store(a.numRegs, std::memory_order_release);
+    return a.numRegs;
+}
+
 int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint8_t *mask, void *y,
                    int32_t *status, cudaStream_t stream)
 {
@@ -292,7 +312,7 @@ int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint
     fp.off_mask = (uint32_t)ns * fp.slot_bytes;
     fp.off_bar = (fp.off_mask + 32u * (uint32_t)ns + 15u) & ~15u;
     const uint32_t smem = fp.off_bar + 16u * (uint32_t)ns;
-    fp.contig_rows = (pl.B == 1 && pl.n_hb == 1) ? 1 : 0;
+    fp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && !long_ranges(pl)) ? 1 : 0;
 
     FwdFn fn = fwd_kernel(pl.dtype, pl.vec);
     static std::atomic<uint64_t> done[4];

@@ -294,7 +294,7 @@ int32_t launch_bwd(const Plan &pl, const Layout &L, const void *gradY, const voi
     mp.w_h = L.w[1];
     mp.m_b = L.m[0];
     mp.m_s = L.m[1];
-    mp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && L.gy[0] == pl.H && L.x[0] == pl.H) ? 1 : 0;
+    mp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && L.gy[0] == pl.H && L.x[0] == pl.H && !long_ranges(pl)) ? 1 : 0;
     mp.w_vec = (L.w[1] == 1 && (L.w[0] * 2) % 16 == 0 && ((uintptr_t)weight & 15u) == 0) ? 1 : 0;
 
     const int R = pl.rows_per_stage;

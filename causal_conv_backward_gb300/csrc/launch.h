@@ -35,6 +35,9 @@ int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_
 
 // Enqueues the forward kernel of plan `p` (dense tensors). `status` is a
 // device word the kernel ORs kErrTimeout into if a wait gives up, or null.
+// Registers per thread of the forward kernel instance for (dtype, vec), from
+// the runtime (0 when unknown).
+int fwd_kernel_regs(int dtype, int vec);
 int32_t launch_fwd(const Plan &p, const void *x, const void *weight, const uint8_t *mask, void *y,
                    int32_t *status, cudaStream_t stream);
 

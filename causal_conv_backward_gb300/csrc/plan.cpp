@@ -74,12 +74,17 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     // each a multiple of 64 halves so every staged row is a multiple of 128 bytes.
     p->n_hb = (int32_t)ceil_div(H, max_hb_width);
     p->hb_width = (int32_t)round_up(ceil_div(H, p->n_hb), 64);
-    // Channels per consumer thread: 8 (16-byte vectors), or 4 when 16-byte
-    // vectors would leave part of the last warp idle and 8-byte vectors fill
-    // whole warps within 4 consumer warps (the case of H-blocks of 384).
+    // Channels per consumer thread: 8 (16-byte vectors), or 4 (8-byte) when
+    // that leaves a smaller share of the consumer lanes idle and needs at most
+    // 5 consumer warps (H-blocks of 384, 576 and 640; wider blocks would give
+    // up their second CTA per SM, which costs more than the idle lanes).
     p->vec = 8;
-    if ((p->hb_width / 8) % 32 != 0 && (p->hb_width / 4) % 32 == 0 && p->hb_width / 4 <= 128)
-        p->vec = 4;
+    {
+        const int64_t v8 = p->hb_width / 8, v4 = p->hb_width / 4;
+        const int64_t w8 = ceil_div(v8, 32), w4 = ceil_div(v4, 32);
+        if (v4 * w8 > v8 * w4 && w4 <= 5)   // v4 / (32 w4) > v8 / (32 w8)
+            p->vec = 4;
+    }
     if (W >= 4)
         p->vec = 4;
     const int vectors = p->hb_width / p->vec;
@@ -107,16 +112,15 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
 
     // Rows per stage and ring depth: the deepest R (fewer barrier round trips)
     // that still leaves a ring of three slots, else the last choice with what
-    // fits. Widths other than 3 have one instance, R = 6. Narrow rows (4
-    // channels per thread) that are copied one row at a time (B > 1 or several
-    // H-blocks) spend most of the producer's time per stage, not per byte, so
-    // long CTA ranges take R = 14 there (2R + W - 1 = 30 copies, one per lane).
+    // fits. Widths other than 3 have one instance, R = 6. Long CTA ranges copy
+    // one row per bulk copy (see long_ranges()); narrow rows (4 channels per
+    // thread) then spend most of the producer's time per stage, not per byte,
+    // so they take R = 14 (2R + W - 1 = 30 copies, one per producer lane).
     int64_t ncta_est = (int64_t)kNumSMs * cps;
     const int64_t rows_all = (int64_t)p->n_hb * B * S;
     if (ncta_est > ceil_div(rows_all, kMinRowsPerCta))
         ncta_est = ceil_div(rows_all, kMinRowsPerCta);
-    const bool row_copies = !(B == 1 && p->n_hb == 1);
-    const bool deep = W == 3 && p->vec == 4 && row_copies && rows_all / ncta_est >= kDeepMinRowsPerCta;
+    const bool deep = W == 3 && p->vec == 4 && rows_all / ncta_est >= kDeepMinRowsPerCta;
     const int r_w3[3] = {8, 6, 4}, r_deep[4] = {14, 8, 6, 4}, r_other[1] = {6};
     const int *r_choices = deep ? r_deep : W == 3 ? r_w3 : r_other;
     const int n_choices = deep ? 4 : W == 3 ? 3 : 1;

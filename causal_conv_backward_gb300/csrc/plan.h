@@ -124,6 +124,12 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
 // Register bound of the backward's main kernel for width W.
 inline int bwd_regs_bound(int64_t W) { return (W >= 4 && W <= kTwoCtaMaxW) ? kRegsTwoCta : kRegsOneCta; }
 
+// CTA ranges of at least kDeepMinRowsPerCta rows stage every row with its own
+// bulk copy, even where a stage's rows lie back to back in memory (B = 1, one
+// H-block): many copies in flight beat one larger copy there. Shorter ranges
+// (small problems) move adjacent rows with one copy per tensor.
+inline bool long_ranges(const Plan &p) { return p.rows_total / p.ncta >= kDeepMinRowsPerCta; }
+
 // First row of CTA c's range.
 MCC1D_HD inline int64_t cta_row_begin(int64_t c, int64_t rows_total, int64_t ncta) {
     return c * rows_total / ncta;

@@ -87,11 +87,14 @@ def test_edge_shapes(S, B, H, dt):
     check_against_oracle(wl, inp, gx, gw, status)
 
 
-# Narrow rows (H = 384, 4 channels per thread) copied one row at a time (B > 1)
-# over long CTA ranges take 14-row stages; these shapes reach that plan, with
-# sequence and CTA-range ends that fall mid-stage.
+# Narrow rows (4 channels per thread: H-blocks of 384, 576 and 640) over long
+# CTA ranges take one bulk copy per row and, at 384, 14-row stages; these
+# shapes reach those plans, with sequence and CTA-range ends that fall
+# mid-stage (H = 1088 splits into two 576-channel blocks).
 DEEP = [(65536, 2, 384, "bf16", ("bernoulli", 0.9)), (16384, 8, 384, "fp16", ("prefix",)),
-        (40001, 3, 384, "bf16", ("spans", 0.2, 64, 1024)), (9001, 13, 384, "fp16", ("none",))]
+        (40001, 3, 384, "bf16", ("spans", 0.2, 64, 1024)), (9001, 13, 384, "fp16", ("none",)),
+        (131072, 1, 384, "fp16", ("bernoulli", 0.8)), (20000, 4, 640, "fp16", ("bernoulli", 0.9)),
+        (3001, 5, 1088, "bf16", ("prefix",))]
 
 
 @pytest.mark.parametrize("S,B,H,dt,mask", DEEP, ids=[f"s{a}_b{b}_h{c}_{d}_{e[0]}" for a, b, c, d, e in DEEP])
