@@ -56,27 +56,29 @@ struct ReduceParams {
     uint8_t *gw;           // [W,H]
     int64_t H;
     int32_t hb_width, ncta, nchunk, W;
+    int32_t splits, lanes_log2;     // splits x (1 << lanes_log2) = kReduceThreads
     int32_t c_lo[kMaxHb], c_hi[kMaxHb], slot_base[kMaxHb];
 };
 
 template <int DT>
-__global__ void __launch_bounds__(kReduceSplits * kReduceLanes) mcc1d_bwd_reduce(const __grid_constant__ ReduceParams p)
+__global__ void __launch_bounds__(kReduceThreads) mcc1d_bwd_reduce(const __grid_constant__ ReduceParams p)
 {
-    __shared__ float4 red[kReduceSplits][kReduceLanes];
+    __shared__ float4 red[kReduceThreads];   // [split][lane]
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int lane = threadIdx.x % kReduceLanes, split = threadIdx.x / kReduceLanes;
+    const int lanes = 1 << p.lanes_log2;
+    const int lane = threadIdx.x & (lanes - 1), split = threadIdx.x >> p.lanes_log2;
     const int b = blockIdx.x;
     const int chunk = b % p.nchunk;
     const int k = (b / p.nchunk) % p.W;
     const int hb = b / (p.nchunk * p.W);
     const int64_t hb0 = (int64_t)hb * p.hb_width;
     const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
-    const int col = chunk * kReduceCols + 4 * lane;
+    const int col = chunk * 4 * lanes + 4 * lane;
     // The H-block's partials are the contiguous slots [base, base + n);
     // split s sums the slice [s*n/S, (s+1)*n/S) in order.
     const int n = p.c_hi[hb] - p.c_lo[hb] + 1;
-    const int sb = (int)((int64_t)split * n / kReduceSplits);
-    const int se = (int)((int64_t)(split + 1) * n / kReduceSplits);
+    const int sb = (int)((int64_t)split * n / p.splits);
+    const int se = (int)((int64_t)(split + 1) * n / p.splits);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (col < width) {
         const float *src = p.part + (((int64_t)p.slot_base[hb] + sb) * p.W + k) * p.hb_width + col;
@@ -90,24 +92,23 @@ __global__ void __launch_bounds__(kReduceSplits * kReduceLanes) mcc1d_bwd_reduce
             acc.w += v.w;
         }
     }
-    red[split][lane] = acc;
+    red[threadIdx.x] = acc;
     __syncthreads();
     // Fixed pairwise tree over the splits.
-#pragma unroll
-    for (int s = kReduceSplits / 2; s >= 1; s >>= 1) {
+    for (int s = p.splits / 2; s >= 1; s >>= 1) {
         if (split < s) {
-            float4 a = red[split][lane];
-            const float4 o = red[split + s][lane];
+            float4 a = red[threadIdx.x];
+            const float4 o = red[threadIdx.x + s * lanes];
             a.x += o.x;
             a.y += o.y;
             a.z += o.z;
             a.w += o.w;
-            red[split][lane] = a;
+            red[threadIdx.x] = a;
         }
         __syncthreads();
     }
     if (split == 0 && col < width) {
-        const float4 a = red[0][lane];
+        const float4 a = red[lane];
         const uint32_t lo = pack2<DT>(make_float2(a.x, a.y));
         const uint32_t hi = pack2<DT>(make_float2(a.z, a.w));
         *reinterpret_cast<uint2 *>(p.gw + 2 * ((int64_t)k * p.H + hb0 + col)) = make_uint2(lo, hi);
@@ -220,7 +221,11 @@ int32_t launch_reduce(const Plan &pl, void *workspace, void *gradWeight, cudaStr
     rp.H = pl.H;
     rp.hb_width = pl.hb_width;
     rp.ncta = pl.ncta;
-    rp.nchunk = (pl.hb_width + kReduceCols - 1) / kReduceCols;
+    rp.nchunk = (pl.hb_width + 4 * pl.red_lanes - 1) / (4 * pl.red_lanes);
+    rp.splits = pl.red_splits;
+    rp.lanes_log2 = 0;
+    while ((1 << rp.lanes_log2) < pl.red_lanes)
+        ++rp.lanes_log2;
     rp.W = pl.W;
     for (int h = 0; h < kMaxHb; ++h) {
         rp.c_lo[h] = pl.c_lo[h];
@@ -233,7 +238,7 @@ int32_t launch_reduce(const Plan &pl, void *workspace, void *gradWeight, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg = {};
     rcfg.gridDim = dim3((unsigned)pl.reduce_blocks);
-    rcfg.blockDim = dim3(kReduceSplits * kReduceLanes);
+    rcfg.blockDim = dim3(kReduceThreads);
     rcfg.dynamicSmemBytes = 0;
     rcfg.stream = stream;
     rcfg.attrs = attr;

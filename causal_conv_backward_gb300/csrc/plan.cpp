@@ -181,7 +181,20 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     p->ws_status_off = kHeaderBytes;
     p->ws_part_off = kHeaderBytes + (uint64_t)round_up(4 * ncta, 256);
     p->ws_bytes = p->ws_part_off + (uint64_t)p->nslots * (uint64_t)W * (uint64_t)p->hb_width * 4u;
-    p->reduce_blocks = (int32_t)(p->n_hb * W * ceil_div(p->hb_width, kReduceCols));
+    // Reduce: each CTA sums red_lanes float4 column groups of one tap over all
+    // partial slots of an H-block, in red_splits contiguous slices (as many as
+    // the slots allow, so no slice is empty on average) and then a fixed
+    // pairwise tree over the slices.
+    int max_slots = 1;
+    for (int hb = 0; hb < p->n_hb; ++hb)
+        if (p->c_hi[hb] - p->c_lo[hb] + 1 > max_slots)
+            max_slots = p->c_hi[hb] - p->c_lo[hb] + 1;
+    int splits = kReduceMinSplits;
+    while (splits < kReduceMaxSplits && 2 * splits <= max_slots)
+        splits *= 2;
+    p->red_splits = splits;
+    p->red_lanes = kReduceThreads / splits;
+    p->reduce_blocks = (int32_t)(p->n_hb * W * ceil_div(p->hb_width, 4 * p->red_lanes));
     return kOk;
 }
 

@@ -31,9 +31,9 @@ constexpr int kHbWidthWide = 2048;    // 4 KB rows, for long CTA ranges
 constexpr int kWideMinRowsPerCta = 1024;
 constexpr int kMinRowsPerCta = 16;    // below this a CTA is not worth its pipeline fill
 constexpr int kFlushStages = 16;      // stages between register -> shared accumulator flushes
-constexpr int kReduceLanes = 8;       // float4 column groups per reduce CTA (32 columns)
-constexpr int kReduceCols = 4 * kReduceLanes;
-constexpr int kReduceSplits = 64;     // contiguous slices of a column's partials per reduce CTA
+constexpr int kReduceThreads = 512;   // threads per reduce CTA: splits x float4 column groups
+constexpr int kReduceMinSplits = 8;   // contiguous slices of a column's partials per reduce CTA:
+constexpr int kReduceMaxSplits = 64;  // the largest power of two <= the slots of an H-block, in range
 constexpr uint64_t kHeaderBytes = 256;
 
 // Status codes, the same values as the public header.
@@ -82,6 +82,7 @@ struct Plan {
     uint64_t ws_status_off, ws_part_off, ws_bytes;
     // Reduce launch.
     int32_t reduce_blocks;
+    int32_t red_splits, red_lanes;   // reduce CTA shape: red_splits x red_lanes = kReduceThreads
 };
 
 // Strides of the inputs in elements (the mask's in bytes), outermost first:
