@@ -75,6 +75,9 @@ def load():
         lib.mcc1d_status_string.restype = ctypes.c_char_p
         lib.mcc1d_version.argtypes = []
         lib.mcc1d_version.restype = i32
+        lib.mcc1d_plan_describe.argtypes = [i64, i64, i64, i64, i32, i32, ctypes.c_char_p, u64,
+                                            ctypes.POINTER(u64)]
+        lib.mcc1d_plan_describe.restype = i32
         _lib = lib
         return lib
 
@@ -218,6 +221,26 @@ def mcc1d_status_string(status: int) -> str:
 
 def mcc1d_version() -> int:
     return int(load().mcc1d_version())
+
+
+PLAN_BWD, PLAN_BWD_EX, PLAN_FWD = 0, 1, 2
+
+
+def mcc1d_plan_describe(S, B, H, W, dtype, kind=PLAN_BWD) -> dict:
+    """The execution plan the library would use for a shape, as a dict
+    (per-H-block ranges ``c_lo``, ``c_hi``, ``slot_base`` as lists)."""
+    lib = load()
+    need = ctypes.c_uint64(0)
+    st = lib.mcc1d_plan_describe(S, B, H, W, dtype_code(dtype), kind, None, 0, ctypes.byref(need))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_plan_describe")
+    buf = ctypes.create_string_buffer(need.value)
+    lib.mcc1d_plan_describe(S, B, H, W, dtype_code(dtype), kind, buf, need.value, None)
+    out = {}
+    for line in buf.value.decode().splitlines():
+        k, v = line.split("=", 1)
+        out[k] = [int(a) for a in v.split(",")] if k in ("c_lo", "c_hi", "slot_base") else int(v)
+    return out
 
 
 def backward(gradY, x, weight, mask=None, *, gradX=None, gradWeight=None, workspace=None,

@@ -4,6 +4,9 @@
 // workspace; nothing touches a device before every check has passed.
 #include <cuda_runtime_api.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <string>
 
 #include "launch.h"
 #include "mcc1d.h"
@@ -213,32 +216,136 @@ extern "C" int32_t mcc1d_bwd_ex(const mcc1d_tensors *t, int64_t S, int64_t B, in
     return launch_bwd(e.plan, e.L, gy, x, t->weight, t->mask, t->gradX, t->gradWeight, workspace, s);
 }
 
+namespace {
+
+// The forward's plan. Its results do not depend on the CTA partition (no
+// reduction), so the plan may use the compiled kernel's register count, asked
+// of the runtime, to keep every CTA resident (no cap when the runtime cannot
+// say, as on a machine without a GPU).
+int32_t fwd_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p)
+{
+    int32_t st = validate_shape(S, B, H, W, dtype);
+    if (st != kOk)
+        return st;
+    st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, 0, p);
+    if (st != kOk)
+        return st;
+    const int regs = fwd_kernel_regs(p->dtype, p->vec);
+    if (regs > 0)
+        st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, regs, p);
+    return st;
+}
+
+}  // namespace
+
 extern "C" int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *mask_or_null, void *y,
                              void *stream, int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
                              int32_t *device_status_or_null)
 {
     if (!x || !weight || !y)
         return kErrNull;
-    Plan p;
     int32_t st = validate_shape(S, B, H, W, dtype);
     if (st != kOk)
         return st;
-    // The forward's results do not depend on the CTA partition (no
-    // reduction), so its plan may use the compiled kernel's register count,
-    // asked of the runtime, to keep every CTA resident.
-    st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, 0, &p);
-    if (st != kOk)
-        return st;
-    const int regs = fwd_kernel_regs(p.dtype, p.vec);
-    if (regs > 0) {
-        st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, regs, &p);
-        if (st != kOk)
-            return st;
-    }
     if (!aligned16(x) || !aligned16(weight) || !aligned16(y))
         return kErrInvalid;
+    Plan p;
+    st = fwd_plan(S, B, H, W, dtype, &p);
+    if (st != kOk)
+        return st;
     return launch_fwd(p, x, weight, mask_or_null, y, device_status_or_null,
                       static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int32_t mcc1d_plan_describe(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                                       int32_t kind, char *buf, uint64_t buf_bytes, uint64_t *needed_out)
+{
+    Plan p;
+    int32_t st;
+    if (kind == MCC1D_PLAN_BWD)
+        st = make_plan(S, B, H, W, dtype, &p);
+    else if (kind == MCC1D_PLAN_BWD_EX)
+        st = make_plan_general(S, B, H, W, dtype, &p);
+    else if (kind == MCC1D_PLAN_FWD)
+        st = fwd_plan(S, B, H, W, dtype, &p);
+    else
+        return kErrInvalid;
+    if (st != kOk)
+        return st;
+    if (kind == MCC1D_PLAN_FWD) {
+        // the forward sizes its own ring and has no workspace or reduce
+        const FwdRing r = fwd_ring(p);
+        p.rows_per_stage = r.rows_per_stage;
+        p.stages = r.stages;
+        p.slot_bytes = r.slot_bytes;
+        p.off_mask = r.off_mask;
+        p.off_bar = r.off_bar;
+        p.off_outer = r.smem_bytes;
+        p.smem_bytes = r.smem_bytes;
+        p.nslots = 0;
+        p.ws_part_off = 0;
+        p.ws_bytes = 0;
+        p.reduce_blocks = 0;
+        p.red_splits = 0;
+        p.red_lanes = 0;
+    }
+    std::string t;
+    auto kv = [&t](const char *k, long long v) {
+        t += k;
+        t += '=';
+        t += std::to_string(v);
+        t += '\n';
+    };
+    auto arr = [&t, &p](const char *k, const int32_t *a) {
+        t += k;
+        t += '=';
+        for (int h = 0; h < p.n_hb; ++h) {
+            if (h)
+                t += ',';
+            t += std::to_string(a[h]);
+        }
+        t += '\n';
+    };
+    kv("S", p.S);
+    kv("B", p.B);
+    kv("H", p.H);
+    kv("W", p.W);
+    kv("dtype", p.dtype);
+    kv("hb_width", p.hb_width);
+    kv("n_hb", p.n_hb);
+    kv("vec", p.vec);
+    kv("consumer_warps", p.consumer_warps);
+    kv("threads", p.threads);
+    kv("rows_per_stage", p.rows_per_stage);
+    kv("stages", p.stages);
+    kv("ctas_per_sm", p.ctas_per_sm);
+    kv("rows_total", p.rows_total);
+    kv("ncta", p.ncta);
+    kv("nslots", p.nslots);
+    kv("row_bytes", p.row_bytes);
+    kv("slot_bytes", p.slot_bytes);
+    kv("off_mask", p.off_mask);
+    kv("off_bar", p.off_bar);
+    kv("off_outer", p.off_outer);
+    kv("smem_bytes", p.smem_bytes);
+    kv("ws_part_off", (long long)p.ws_part_off);
+    kv("ws_bytes", (long long)p.ws_bytes);
+    kv("reduce_blocks", p.reduce_blocks);
+    kv("red_splits", p.red_splits);
+    kv("red_lanes", p.red_lanes);
+    kv("regs_bound", kind == MCC1D_PLAN_FWD ? 0 : bwd_regs_bound(W));
+    kv("long_ranges", long_ranges(p) ? 1 : 0);
+    arr("c_lo", p.c_lo);
+    arr("c_hi", p.c_hi);
+    arr("slot_base", p.slot_base);
+    if (needed_out)
+        *needed_out = t.size() + 1;
+    if (buf && buf_bytes > 0) {
+        const size_t n = t.size() < buf_bytes - 1 ? t.size() : (size_t)(buf_bytes - 1);
+        memcpy(buf, t.data(), n);
+        buf[n] = '\0';
+    }
+    return kOk;
 }
 
 extern "C" int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *status_out)

@@ -263,6 +263,29 @@ static FwdFn fwd_kernel(int dtype, int vec)
     return vec == 4 ? mcc1d_fwd_main<1, kFwdR, 2> : mcc1d_fwd_main<1, kFwdR, 4>;
 }
 
+FwdRing fwd_ring(const Plan &pl)
+{
+    // kFwdR output rows plus the two halo rows per slot; as many slots as the
+    // CTA's share of shared memory allows, 2 .. kFwdMaxStages
+    FwdRing r;
+    r.rows_per_stage = kFwdR;
+    r.slot_bytes = (uint32_t)(kFwdR + 2) * pl.row_bytes;
+    int64_t budget = kSmemPerSM / pl.ctas_per_sm - kSmemReservedPerCta;
+    if (budget > kSmemDynMax)
+        budget = kSmemDynMax;
+    budget -= 64;
+    int64_t ns = budget / (r.slot_bytes + 48);
+    if (ns > kFwdMaxStages)
+        ns = kFwdMaxStages;
+    if (ns < 2)
+        ns = 2;
+    r.stages = (int32_t)ns;
+    r.off_mask = (uint32_t)ns * r.slot_bytes;
+    r.off_bar = (r.off_mask + 32u * (uint32_t)ns + 15u) & ~15u;
+    r.smem_bytes = r.off_bar + 16u * (uint32_t)ns;
+    return r;
+}
+
 int fwd_kernel_regs(int dtype, int vec)
 {
     // registers per thread of the forward instance (cached per device and
@@ -301,17 +324,12 @@ int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint
     fp.hb_width = pl.hb_width;
     fp.ncta = pl.ncta;
     fp.row_bytes = pl.row_bytes;
-    fp.slot_bytes = (uint32_t)(kFwdR + 2) * pl.row_bytes;
-    const int64_t budget = kSmemPerSM / pl.ctas_per_sm - kSmemReservedPerCta - 64;
-    int64_t ns = budget / (fp.slot_bytes + 48);
-    if (ns > kFwdMaxStages)
-        ns = kFwdMaxStages;
-    if (ns < 2)
-        ns = 2;
-    fp.stages = (int32_t)ns;
-    fp.off_mask = (uint32_t)ns * fp.slot_bytes;
-    fp.off_bar = (fp.off_mask + 32u * (uint32_t)ns + 15u) & ~15u;
-    const uint32_t smem = fp.off_bar + 16u * (uint32_t)ns;
+    const FwdRing ring = fwd_ring(pl);
+    fp.slot_bytes = ring.slot_bytes;
+    fp.stages = ring.stages;
+    fp.off_mask = ring.off_mask;
+    fp.off_bar = ring.off_bar;
+    const uint32_t smem = ring.smem_bytes;
     fp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && !long_ranges(pl)) ? 1 : 0;
 
     FwdFn fn = fwd_kernel(pl.dtype, pl.vec);
@@ -324,7 +342,7 @@ int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint
     if (!(done[slot_id].load(std::memory_order_acquire) & bit)) {
         if (cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemPerCtaMax - 1024) != cudaSuccess)
+                                 kSmemDynMax) != cudaSuccess)
             return kErrCuda;
         done[slot_id].fetch_or(bit, std::memory_order_acq_rel);
     }

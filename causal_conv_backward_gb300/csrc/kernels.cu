@@ -204,7 +204,7 @@ static bool ensure_smem_attr(const void *fn)
         return true;
     // leave room for the kernel's few bytes of static shared memory
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemPerCtaMax - 1024) != cudaSuccess)
+                             kSmemDynMax) != cudaSuccess)
         return false;
     devmask[slot] |= bit;
     return true;

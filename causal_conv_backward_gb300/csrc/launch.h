@@ -35,6 +35,13 @@ int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_
 
 // Enqueues the forward kernel of plan `p` (dense tensors). `status` is a
 // device word the kernel ORs kErrTimeout into if a wait gives up, or null.
+// The forward's shared-memory ring for plan `p` (its own rows per stage and
+// depth; the backward's ring fields of the plan do not apply to it).
+struct FwdRing {
+    int32_t rows_per_stage, stages;
+    uint32_t slot_bytes, off_mask, off_bar, smem_bytes;
+};
+FwdRing fwd_ring(const Plan &p);
 // Registers per thread of the forward kernel instance for (dtype, vec), from
 // the runtime (0 when unknown).
 int fwd_kernel_regs(int dtype, int vec);

@@ -108,7 +108,9 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
 
     p->row_bytes = (uint32_t)p->hb_width * 2u;
     const uint32_t outer_bytes = (uint32_t)p->consumer_warps * 32u * (uint32_t)W * (uint32_t)p->vec * 4u;
-    const int64_t budget = kSmemPerSM / cps - kSmemReservedPerCta;
+    int64_t budget = kSmemPerSM / cps - kSmemReservedPerCta;
+    if (budget > kSmemDynMax)
+        budget = kSmemDynMax;
 
     // Rows per stage and ring depth: the deepest R (fewer barrier round trips)
     // that still leaves a ring of three slots, else the last choice with what

@@ -25,6 +25,10 @@ constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs
 constexpr int kSmemPerSM = 233472;    // 228 KB of shared memory per SM
 constexpr int kSmemPerCtaMax = 232448;// 227 KB opt-in maximum per CTA
 constexpr int kSmemReservedPerCta = 1024;
+// Dynamic shared memory a kernel may be given: the opt-in maximum less room
+// for the kernels' few bytes of static shared memory. The launch attribute is
+// set to this, and no plan budgets a CTA more.
+constexpr int kSmemDynMax = kSmemPerCtaMax - 1024;
 constexpr int kMaxHb = 64;            // upper bound on H-blocks recorded in a plan
 constexpr int kHbWidthNarrow = 1024;  // halves per H-block: 2 KB rows
 constexpr int kHbWidthWide = 2048;    // 4 KB rows, for long CTA ranges

@@ -227,7 +227,7 @@ int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *st
  *
  *  - A shape whose mcc1d_bwd_workspace_size exceeds MCC1D_NOALLOC_SCRATCH_BYTES
  *    is rejected with MCC1D_ERR_WORKSPACE before anything is enqueued. Every
- *    shape within the limits above needs at most about 6.7 MB, so all of them
+ *    shape within the limits above needs at most about 4.7 MB, so all of them
  *    fit; the check guards against a future plan needing more.
  *  - All calls on a device share the one array. Calls that may overlap on the
  *    GPU (different streams, or host threads with no ordering between them)
@@ -272,6 +272,22 @@ int32_t mcc1d_bwd_noalloc(const void *gradY, const void *x, const void *weight,
 int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *mask_or_null, void *y,
                   void *stream, int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
                   int32_t *device_status_or_null);
+
+/*
+ * Diagnostics (no counterpart on the page): the execution plan the library
+ * would use for a shape, as text lines "key=value" (H-block split, channels
+ * per thread, warps, rows per stage, ring depth, CTAs, shared memory,
+ * workspace layout, reduce shape; per-H-block CTA and slot ranges as comma
+ * lists). kind: MCC1D_PLAN_BWD (mcc1d_bwd, W = 3), MCC1D_PLAN_BWD_EX (the
+ * strided calls, 1 <= W <= 8) or MCC1D_PLAN_FWD (mcc1d_fwd; with a GPU the
+ * forward's plan also depends on its kernel's register count). Writes at most
+ * buf_bytes - 1 characters plus a terminating NUL to buf (buf may be NULL);
+ * *needed_out (optional) receives the full length + 1. Host only; shape
+ * errors as mcc1d_bwd_workspace_size, MCC1D_ERR_PARAM_INVALID for a bad kind.
+ */
+enum { MCC1D_PLAN_BWD = 0, MCC1D_PLAN_BWD_EX = 1, MCC1D_PLAN_FWD = 2 };
+int32_t mcc1d_plan_describe(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
+                            int32_t kind, char *buf, uint64_t buf_bytes, uint64_t *needed_out);
 
 /* Static text for a status code; never NULL. */
 const char *mcc1d_status_string(int32_t status);

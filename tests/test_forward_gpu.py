@@ -61,7 +61,8 @@ EDGE = []
 for dt in ("bf16", "fp16"):
     for S in (1, 2, 3, 4, 5, 9, 64, 65, 129):
         EDGE.append((S, 1, 384, dt))
-    for (S, B, H) in ((3, 5, 1088), (33, 2, 2112), (7, 32, 1024), (9, 2, 24576), (1000, 3, 448)):
+    for (S, B, H) in ((3, 5, 1088), (33, 2, 2112), (7, 32, 1024), (9, 2, 24576), (1000, 3, 448),
+                      (700, 3, 1920), (20000, 2, 768), (30000, 1, 640)):
         EDGE.append((S, B, H, dt))
 
 

@@ -105,6 +105,20 @@ def test_narrow_deep_stages(S, B, H, dt, mask):
     check_against_oracle(wl, inp, gx, gw, status)
 
 
+# H-blocks of 1920 channels with one CTA per SM (long CTA ranges): the ring
+# that fits the SM's whole shared memory must also fit the per-kernel dynamic
+# limit (these plans once asked for more and failed to launch).
+WIDE = [(40000, 4, 1920, "bf16"), (20000, 4, 3840, "fp16")]
+
+
+@pytest.mark.parametrize("S,B,H,dt", WIDE, ids=[f"s{a}_b{b}_h{c}_{d}" for a, b, c, d in WIDE])
+def test_wide_blocks_one_cta_per_sm(S, B, H, dt):
+    wl = datagen.Workload("wide", S, B, H, dt, mask=("bernoulli", 0.9))
+    inp = datagen.generate(wl, seed=H)
+    gx, gw, status, _ = run_cuda(inp, S, B, H, dt)
+    check_against_oracle(wl, inp, gx, gw, status)
+
+
 def test_page_sample_zeros():
     """The operator page's call example: S=1, B=2, H=384, fp16, every input
     zero and a mask of zero bytes: both outputs are zero."""
