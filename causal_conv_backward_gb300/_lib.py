@@ -78,6 +78,8 @@ def load():
         lib.mcc1d_plan_describe.argtypes = [i64, i64, i64, i64, i32, i32, ctypes.c_char_p, u64,
                                             ctypes.POINTER(u64)]
         lib.mcc1d_plan_describe.restype = i32
+        lib.mcc1d_selftest_wait.argtypes = [vp, i32, vp]
+        lib.mcc1d_selftest_wait.restype = i32
         _lib = lib
         return lib
 
@@ -221,6 +223,17 @@ def mcc1d_status_string(status: int) -> str:
 
 def mcc1d_version() -> int:
     return int(load().mcc1d_version())
+
+
+def mcc1d_selftest_wait(device_status, arrive: bool, stream=None) -> None:
+    """Enqueue the bounded-wait self-test; ``device_status`` is an int32 device
+    word (a tensor or pointer) that receives MCC1D_OK or
+    MCC1D_ERR_DEVICE_TIMEOUT."""
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = load().mcc1d_selftest_wait(_ptr(device_status), 1 if arrive else 0, stream or None)
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_selftest_wait")
 
 
 PLAN_BWD, PLAN_BWD_EX, PLAN_FWD = 0, 1, 2

@@ -348,6 +348,15 @@ extern "C" int32_t mcc1d_plan_describe(int64_t S, int64_t B, int64_t H, int64_t 
     return kOk;
 }
 
+extern "C" int32_t mcc1d_selftest_wait(int32_t *device_status, int32_t arrive, void *stream)
+{
+    if (!device_status)
+        return kErrNull;
+    if (((uintptr_t)device_status & 3u) != 0)
+        return kErrInvalid;
+    return launch_wait_selftest(device_status, arrive, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *status_out)
 {
     if (!workspace || !status_out)

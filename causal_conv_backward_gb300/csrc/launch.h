@@ -42,6 +42,10 @@ struct FwdRing {
     uint32_t slot_bytes, off_mask, off_bar, smem_bytes;
 };
 FwdRing fwd_ring(const Plan &p);
+// One thread waiting on an mbarrier with the library's bounded wait; writes
+// kOk (arrive != 0: it arrives first) or kErrTimeout (nothing arrives) to the
+// device word `status`.
+int32_t launch_wait_selftest(int32_t *status, int32_t arrive, cudaStream_t stream);
 // Registers per thread of the forward kernel instance for (dtype, vec), from
 // the runtime (0 when unknown).
 int fwd_kernel_regs(int dtype, int vec);

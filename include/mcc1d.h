@@ -289,6 +289,20 @@ enum { MCC1D_PLAN_BWD = 0, MCC1D_PLAN_BWD_EX = 1, MCC1D_PLAN_FWD = 2 };
 int32_t mcc1d_plan_describe(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
                             int32_t kind, char *buf, uint64_t buf_bytes, uint64_t *needed_out);
 
+/*
+ * Self-test of the bounded device-side wait (no counterpart on the page).
+ * Every wait inside the library's kernels gives up after about 2 s and turns
+ * into MCC1D_ERR_DEVICE_TIMEOUT instead of hanging the GPU. This call runs
+ * that same wait in one thread on `stream`: with arrive != 0 the thread
+ * signals the barrier first and MCC1D_OK is written to *device_status; with
+ * arrive == 0 nothing ever signals it, the wait runs out (about 2 s) and
+ * MCC1D_ERR_DEVICE_TIMEOUT is written. The context stays usable afterwards.
+ * device_status: a 4-byte-aligned device (or device-accessible) int32.
+ * Asynchronous; MCC1D_ERR_PARAM_NULLPTR / MCC1D_ERR_PARAM_INVALID for a null
+ * or misaligned pointer, MCC1D_ERR_CUDA if the launch fails.
+ */
+int32_t mcc1d_selftest_wait(int32_t *device_status, int32_t arrive, void *stream);
+
 /* Static text for a status code; never NULL. */
 const char *mcc1d_status_string(int32_t status);
 
