@@ -227,12 +227,13 @@ int32_t fwd_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan
     int32_t st = validate_shape(S, B, H, W, dtype);
     if (st != kOk)
         return st;
-    st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, 0, p);
+    PlanOpts o = {kFwdConsumerWarpsPerSM, kHbWidthWide, 0, 8, true};
+    st = make_plan_for(S, B, H, W, dtype, o, p);
     if (st != kOk)
         return st;
-    const int regs = fwd_kernel_regs(p->dtype, p->vec);
-    if (regs > 0)
-        st = make_plan_for(S, B, H, W, dtype, kFwdConsumerWarpsPerSM, kHbWidthWide, regs, p);
+    o.regs_bound = fwd_kernel_regs(p->dtype, p->vec);
+    if (o.regs_bound > 0)
+        st = make_plan_for(S, B, H, W, dtype, o, p);
     return st;
 }
 

@@ -49,17 +49,20 @@ int32_t make_plan_general(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dt
     // fit the two-CTA register bound, and sixteen consumer warps per SM hide
     // the longer arithmetic of each row.
     if (W >= 4)
-        return make_plan_for(S, B, H, W, dtype, W <= kTwoCtaMaxW ? 16 : 8, kHbWidthNarrow,
-                             bwd_regs_bound(W), p);
-    const int32_t st = make_plan_for(S, B, H, W, dtype, 8, kHbWidthWide, bwd_regs_bound(W), p);
+        return make_plan_for(S, B, H, W, dtype,
+                             {W <= kTwoCtaMaxW ? 16 : 8, kHbWidthNarrow, bwd_regs_bound(W), 5, false}, p);
+    const int32_t st = make_plan_for(S, B, H, W, dtype, {8, kHbWidthWide, bwd_regs_bound(W), 5, false}, p);
     if (st != kOk || p->rows_total / p->ncta >= kWideMinRowsPerCta)
         return st;
-    return make_plan_for(S, B, H, W, dtype, 8, kHbWidthNarrow, bwd_regs_bound(W), p);
+    return make_plan_for(S, B, H, W, dtype, {8, kHbWidthNarrow, bwd_regs_bound(W), 5, false}, p);
 }
 
-int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
-                      int target_consumer_warps, int max_hb_width, int regs_bound, Plan *p)
+int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, const PlanOpts &o,
+                      Plan *p)
 {
+    const int target_consumer_warps = o.target_consumer_warps;
+    const int max_hb_width = o.max_hb_width;
+    const int regs_bound = o.regs_bound;
     int32_t st = validate_shape_w(S, B, H, W, dtype);
     if (st != kOk)
         return st;
@@ -74,15 +77,19 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     // each a multiple of 64 halves so every staged row is a multiple of 128 bytes.
     p->n_hb = (int32_t)ceil_div(H, max_hb_width);
     p->hb_width = (int32_t)round_up(ceil_div(H, p->n_hb), 64);
-    // Channels per consumer thread: 8 (16-byte vectors), or 4 (8-byte) when
-    // that leaves a smaller share of the consumer lanes idle and needs at most
-    // 5 consumer warps (H-blocks of 384, 576 and 640; wider blocks would give
-    // up their second CTA per SM, which costs more than the idle lanes).
+    // Channels per consumer thread: 8 (16-byte vectors), or 4 (8-byte) within
+    // o.vec4_max_warps consumer warps, either always (the forward: twice the
+    // threads in flight per row, at 69 registers against 96; H-blocks up to
+    // 1024) or when that leaves a smaller share of the consumer lanes idle
+    // (the backward, within 5 warps: H-blocks of 384, 576 and 640; wider
+    // blocks would give up their second CTA per SM, which costs more than the
+    // idle lanes).
     p->vec = 8;
     {
         const int64_t v8 = p->hb_width / 8, v4 = p->hb_width / 4;
         const int64_t w8 = ceil_div(v8, 32), w4 = ceil_div(v4, 32);
-        if (v4 * w8 > v8 * w4 && w4 <= 5)   // v4 / (32 w4) > v8 / (32 w8)
+        const bool better_lanes = v4 * w8 > v8 * w4;   // v4 / (32 w4) > v8 / (32 w8)
+        if (w4 <= o.vec4_max_warps && (o.vec4_always || better_lanes))
             p->vec = 4;
     }
     if (W >= 4)

@@ -122,10 +122,17 @@ int32_t validate_shape_w(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dty
 int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p);
 // The backward's plan for any width 1 <= W <= kMaxW (the strided entry points).
 int32_t make_plan_general(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p);
-// regs_bound: the register bound the kernel is compiled under; CTAs per SM
-// never exceed what the register file holds at that bound (0: no cap).
-int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
-                      int target_consumer_warps, int max_hb_width, int regs_bound, Plan *p);
+// What a kernel asks of its plan.
+struct PlanOpts {
+    int target_consumer_warps;   // consumer warps per SM to aim for
+    int max_hb_width;            // widest H-block (channels)
+    int regs_bound;              // registers per thread the kernel is held to; CTAs per SM
+                                 // never exceed what the register file holds (0: no cap)
+    int vec4_max_warps;          // 4 channels per thread allowed up to this many consumer warps
+    bool vec4_always;            // ... and taken whenever allowed (else only for better lane use)
+};
+int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, const PlanOpts &o,
+                      Plan *p);
 // Register bound of the backward's main kernel for width W.
 inline int bwd_regs_bound(int64_t W) { return (W >= 4 && W <= kTwoCtaMaxW) ? kRegsTwoCta : kRegsOneCta; }
 
