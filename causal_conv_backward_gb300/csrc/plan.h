@@ -1,8 +1,11 @@
-// plan.h - shape validation and the launch plan of the backward (host only).
+// plan.h - shape validation and the launch plans (host only).
 //
-// The plan is a pure function of (S, B, H, dtype): the partition of the work,
-// the order of every floating-point sum and the workspace size never depend on
-// the device it later runs on, so equal inputs give bitwise-equal outputs.
+// The backward's plan is a pure function of (S, B, H, W, dtype): the partition
+// of the work, the order of every floating-point sum and the workspace size
+// never depend on the device it later runs on, so equal inputs give
+// bitwise-equal outputs. The forward's plan may also use its kernel's register
+// count as the runtime reports it: each of its outputs is one thread's sum,
+// so its results do not depend on the partition.
 #pragma once
 
 #include <stdint.h>
@@ -117,8 +120,8 @@ int32_t validate_shape_w(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dty
 // Fills *p for a valid shape; returns the validate_shape status otherwise.
 // make_plan is the backward's plan: 8 consumer warps per SM (its register
 // budget), and 4 KB H-block rows when every CTA range is long enough for the
-// larger copies to pay, else 2 KB. make_plan_for fixes both choices (the
-// forward, at about 96 registers a thread, asks for more warps).
+// larger copies to pay, else 2 KB. make_plan_for takes those choices from a
+// PlanOpts (the forward asks for 16 consumer warps and 4 KB rows).
 int32_t make_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p);
 // The backward's plan for any width 1 <= W <= kMaxW (the strided entry points).
 int32_t make_plan_general(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p);
