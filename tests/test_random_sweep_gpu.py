@@ -10,7 +10,8 @@ memory, an H-slice of a wider buffer, every other element along H), of the
 weight ([H,W] memory) and of the mask ([S,B] memory). W = 3 on dense tensors
 goes through mcc1d_bwd, everything else through mcc1d_bwd_ex. The plan's
 edge cases (H-block splits, CTA ranges that end mid-sequence or mid-batch,
-ragged stages, gathered inputs) are hit by chance many times over.
+ragged stages, gathered inputs) are hit by chance many times over. Each case
+runs twice with differently filled workspaces and must give the same bits.
 """
 import numpy as np
 import pytest
@@ -102,18 +103,25 @@ def test_random_case(n):
     gw = torch.full((W, H), float("nan"), dtype=gy.dtype, device="cuda")
     stream = torch.cuda.current_stream()
     dense = W == 3 and c["layout"] == "sbh" and not c["w_t"] and not c["m_t"]
-    if dense:
-        nb = m.mcc1d_bwd_workspace_size(S, B, H, W, dt, mask is not None)
-        ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
-        m.mcc1d_bwd(gy_v, x_v, w, mask, gx, gw, ws, stream, S, B, H, W, dt, nb)
-    else:
-        t = m.tensors(gy_v, x_v, w, mask, gx, gw)
-        nb = m.mcc1d_bwd_ex_workspace_size(t, S, B, H, W, dt)
-        ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
-        m.mcc1d_bwd_ex(t, S, B, H, W, dt, ws, nb, stream)
-    assert m.mcc1d_bwd_device_status(ws, stream) == 0
-    gxb = gx.view(torch.int16).cpu().numpy().view(np.uint16)
-    gwb = gw.view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def call(fill):
+        """One call with the workspace pre-filled with `fill` bytes."""
+        if dense:
+            nb = m.mcc1d_bwd_workspace_size(S, B, H, W, dt, mask is not None)
+            ws = torch.full((nb,), fill, dtype=torch.uint8, device="cuda")
+            m.mcc1d_bwd(gy_v, x_v, w, mask, gx, gw, ws, stream, S, B, H, W, dt, nb)
+        else:
+            t = m.tensors(gy_v, x_v, w, mask, gx, gw)
+            nb = m.mcc1d_bwd_ex_workspace_size(t, S, B, H, W, dt)
+            ws = torch.full((nb,), fill, dtype=torch.uint8, device="cuda")
+            m.mcc1d_bwd_ex(t, S, B, H, W, dt, ws, nb, stream)
+        assert m.mcc1d_bwd_device_status(ws, stream) == 0
+        return (gx.view(torch.int16).cpu().numpy().view(np.uint16).copy(),
+                gw.view(torch.int16).cpu().numpy().view(np.uint16).copy())
+
+    gxb, gwb = call(0xFF)
+    gx2, gw2 = call(0x00)   # deterministic: a second call with other workspace garbage
+    assert np.array_equal(gxb, gx2) and np.array_equal(gwb, gw2)
     ref = oracle.bwd(S, B, H, W, dt, inp["gy"], inp["x"], inp["w"], inp["mask"], want_exact=True)
     ulp = max_ulp(gxb, ref["gx"])
     assert ulp <= GX_MAX_ULP, f"gradX off by {ulp} ulp"
