@@ -165,8 +165,8 @@ def workload(name: str, no_mask: bool):
 
 
 def chosen_workload(args):
-    if args.W != 3 and args.op == "fwd":
-        raise SystemExit("bench.py: the forward runs at W = 3 only")
+    if args.op == "fwd" and args.layout != "sbh":
+        raise SystemExit("bench.py: the forward takes dense [S,B,H] tensors only")
     wl = workload(args.workload, args.no_mask)
     if args.seq_len:
         wl = wl.resized(S=args.seq_len)
@@ -330,7 +330,7 @@ def gpu_arm(args):
         def step(st=None):  # noqa: F811
             m.mcc1d_fwd(x, w, mask, y, st or stream, wl.S, wl.B, wl.H, wl.W, code)
 
-    if args.layout == "bsh" or wl.W != 3:
+    if args.op == "bwd" and (args.layout == "bsh" or wl.W != 3):
         # bsh: the same values held as [B,S,H] buffers and passed as strided
         # views; other widths: the strided call with dense strides
         gy_v = gy.transpose(0, 1).contiguous().transpose(0, 1) if args.layout == "bsh" else gy

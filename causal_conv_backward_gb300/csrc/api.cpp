@@ -224,14 +224,17 @@ namespace {
 // say, as on a machine without a GPU).
 int32_t fwd_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan *p)
 {
-    int32_t st = validate_shape(S, B, H, W, dtype);
+    int32_t st = validate_shape_w(S, B, H, W, dtype);
     if (st != kOk)
         return st;
-    PlanOpts o = {kFwdConsumerWarpsPerSM, kHbWidthWide, 0, 8, true};
+    // W = 3: blocks of up to 2048 channels, 8 or 4 per thread; other widths
+    // keep their W weights and W-1 window rows per channel in registers with
+    // 4 channels per thread and blocks of up to 1024 channels
+    PlanOpts o = {kFwdConsumerWarpsPerSM, W == 3 ? kHbWidthWide : kHbWidthNarrow, 0, 8, true};
     st = make_plan_for(S, B, H, W, dtype, o, p);
     if (st != kOk)
         return st;
-    o.regs_bound = fwd_kernel_regs(p->dtype, p->vec);
+    o.regs_bound = fwd_kernel_regs(p->dtype, p->vec, p->W);
     if (o.regs_bound > 0)
         st = make_plan_for(S, B, H, W, dtype, o, p);
     return st;
@@ -245,7 +248,7 @@ extern "C" int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *m
 {
     if (!x || !weight || !y)
         return kErrNull;
-    int32_t st = validate_shape(S, B, H, W, dtype);
+    int32_t st = validate_shape_w(S, B, H, W, dtype);
     if (st != kOk)
         return st;
     if (!aligned16(x) || !aligned16(weight) || !aligned16(y))

@@ -2,17 +2,19 @@
 //
 // The forward of the operator whose gradient mcc1d_bwd computes (the CANN
 // page "aclnnMaskedCausalConv1dBackward" names it MaskedCausalConv1d and
-// calls the mask the convolution's output mask): for every channel h,
-//   y(t,j) = mask(j,t) * (w(0)*x(t-2,j) + w(1)*x(t-1,j) + w(2)*x(t,j))
+// calls the mask the convolution's output mask): for every channel h and
+// kernel width W (3 on the page),
+//   y(t,j) = mask(j,t) * sum_{k<W} w(k) * x(t-(W-1)+k, j)
+//          (W = 3: w(0)*x(t-2) + w(1)*x(t-1) + w(2)*x(t))
 // with x zero before t = 0. Transposing this map gives exactly the page's
 // gradX and gradWeight formulas.
 //
-// Same streaming design as the backward, with the two-row halo behind each
+// Same streaming design as the backward, with the W-1-row halo behind each
 // row instead of ahead: per stage the producer warp copies x rows t .. t+R-1
-// (plus t-2, t-1 when a sequence or CTA range starts) into a ring slot with
-// cp.async.bulk and stores the stage's output-mask bytes; consumer threads
-// keep x(t-2), x(t-1) in registers, form y with the compensated three-term
-// sum and a 16-byte streaming store. No reduction, no workspace.
+// (plus t-(W-1) .. t-1 when a sequence or CTA range starts) into a ring slot
+// with cp.async.bulk and stores the stage's output-mask bytes; consumer
+// threads keep the last W-1 x rows in registers, form y with the compensated
+// W-term sum and a streaming store. No reduction, no workspace.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -32,7 +34,7 @@ constexpr int kFwdMaxStages = 8;
 
 struct FwdParams {
     const uint8_t *x;      // [S,B,H] 16-bit, addressed in bytes
-    const uint16_t *w;     // [3,H]
+    const uint16_t *w;     // [W,H]
     const uint8_t *mask;   // [B,S] or null
     uint8_t *y;            // [S,B,H]
     int32_t *status;       // device word or null: set to kErrTimeout if a wait gives up
@@ -42,17 +44,17 @@ struct FwdParams {
     int32_t contig_rows;
 };
 
-// Byte q of a stage (row cursor at output row t = c.i): q = 0, 1 say whether
-// the halo rows t-2, t-1 exist (t-2+q >= 0); q >= 2 is the output mask of row
-// t+q-2 (zero past the end of S).
-template <int R>
+// Byte q of a stage (row cursor at output row t = c.i): q < W-1 says whether
+// the halo row t-(W-1)+q exists (is >= 0); q >= W-1 is the output mask of row
+// t+q-(W-1) (zero past the end of S).
+template <int R, int W>
 __device__ __forceinline__ uint32_t fwd_stage_byte(const FwdParams &p, const Cursor &c, int lane)
 {
-    if (lane < 2)
-        return c.i - 2 + lane >= 0 ? 1u : 0u;
-    if (lane >= R + 2)
+    if (lane < W - 1)
+        return c.i - (W - 1) + lane >= 0 ? 1u : 0u;
+    if (lane >= R + W - 1)
         return 0;
-    const int64_t row = c.i + lane - 2;
+    const int64_t row = c.i + lane - (W - 1);
     if (row >= p.S)
         return 0;
     if (p.mask == nullptr)
@@ -60,7 +62,7 @@ __device__ __forceinline__ uint32_t fwd_stage_byte(const FwdParams &p, const Cur
     return __ldg(p.mask + (int64_t)c.j * p.S + row) != 0 ? 1u : 0u;
 }
 
-template <int R>
+template <int R, int W>
 __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64_t r1, int lane)
 {
     const int NS = p.stages;
@@ -73,7 +75,7 @@ __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64
     int slot = 0, stage = 0;
     uint32_t ph = 0;
     bool dead = false;
-    uint32_t mnext = fwd_stage_byte<R>(p, cur, lane);
+    uint32_t mnext = fwd_stage_byte<R, W>(p, cur, lane);
     while (cur.pos < r1) {
         const int n = cur.rows<R>(p.S);
         const bool head = (stage == 0) || (cur.i == 0);
@@ -84,22 +86,22 @@ __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             if (dead)
                 break;
         }
-        if (lane < R + 2)
+        if (lane < R + W - 1)
             smem[p.off_mask + 32u * slot + lane] = (uint8_t)mcur;
         {
             Cursor nx = cur;
             nx.advance(n, p.S, p.B);
             if (nx.pos < r1)
-                mnext = fwd_stage_byte<R>(p, nx, lane);
+                mnext = fwd_stage_byte<R, W>(p, nx, lane);
         }
         const int64_t hb0 = (int64_t)cur.hb * p.hb_width;
         const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
         const uint32_t wbytes = (uint32_t)width * 2u;
-        // slot row q holds x row t-2+q; the stage loads q in [q0, n+2)
-        int q0 = 2;
+        // slot row q holds x row t-(W-1)+q; the stage loads q in [q0, n+W-1)
+        int q0 = W - 1;
         if (head)
-            q0 = cur.i >= 2 ? 0 : (int)(2 - cur.i);
-        const int nrows = n + 2 - q0;
+            q0 = cur.i >= W - 1 ? 0 : (int)(W - 1 - cur.i);
+        const int nrows = n + W - 1 - q0;
         __syncwarp();
         if (lane == 0)
             mbar_arrive_expect_tx(bar_full0 + 8u * slot, (uint32_t)nrows * wbytes);
@@ -107,11 +109,11 @@ __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64
         const uint32_t slot_base = ring0 + (uint32_t)slot * p.slot_bytes;
         if (p.contig_rows) {
             if (lane == 0)
-                bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.x + 2 * (cur.i - 2 + q0) * p.H,
+                bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.x + 2 * (cur.i - (W - 1) + q0) * p.H,
                          (uint32_t)nrows * wbytes, bar_full0 + 8u * slot);
         } else if (lane < nrows) {
             const int q = q0 + lane;
-            const int64_t e = (cur.i - 2 + q) * row_elems + (int64_t)cur.j * p.H + hb0;
+            const int64_t e = (cur.i - (W - 1) + q) * row_elems + (int64_t)cur.j * p.H + hb0;
             bulk_g2s(slot_base + (uint32_t)q * p.row_bytes, p.x + 2 * e, wbytes, bar_full0 + 8u * slot);
         }
         cur.advance(n, p.S, p.B);
@@ -130,10 +132,11 @@ __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64
     return __any_sync(0xFFFFFFFFu, dead);
 }
 
-template <int DT, int R, int NP>
+template <int DT, int R, int NP, int W>
 __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64_t r1, int ct, int lane)
 {
     constexpr int CH = 2 * NP;
+    constexpr int WH = W - 1;                  // rows of the window
     const int NS = p.stages;
     const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
@@ -142,10 +145,13 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
     cur.init(r0, r1, p.S, p.BS);
     int hb_cur = -1;
     bool active = false;
-    Vf<NP> w0, w1, w2, g0, g1;
+    Vf<NP> wt[W];                    // weight rows k = 0 .. W-1 of this thread's channels
+    Vf<NP> win[WH > 0 ? WH : 1];     // x(t-(W-1)) .. x(t-1) for the next row t
 #pragma unroll
-    for (int e = 0; e < NP; ++e)
-        g0.e[e] = g1.e[e] = make_float2(0.f, 0.f);
+    for (int q = 0; q < (WH > 0 ? WH : 1); ++q)
+#pragma unroll
+        for (int e = 0; e < NP; ++e)
+            win[q].e[e] = make_float2(0.f, 0.f);
     int slot = 0, stage = 0;
     uint32_t ph = 0;
     bool dead = false;
@@ -158,9 +164,9 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
             active = CH * ct < width;
             if (active) {
-                w0 = unpack<DT, NP>(ldg_raw<NP>(p.w + 0 * p.H + hb0 + CH * ct));
-                w1 = unpack<DT, NP>(ldg_raw<NP>(p.w + 1 * p.H + hb0 + CH * ct));
-                w2 = unpack<DT, NP>(ldg_raw<NP>(p.w + 2 * p.H + hb0 + CH * ct));
+#pragma unroll
+                for (int k = 0; k < W; ++k)
+                    wt[k] = unpack<DT, NP>(ldg_raw<NP>(p.w + k * p.H + hb0 + CH * ct));
             }
         }
         if (!dead) {
@@ -172,30 +178,50 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             const uint8_t *xs = smem + (size_t)slot * p.slot_bytes + 2 * CH * ct;
             const uint8_t *ms = smem + p.off_mask + 32u * slot;
             if (head) {
-                g0 = load_masked<DT, NP>(xs, ms[0]);
-                g1 = load_masked<DT, NP>(xs + p.row_bytes, ms[1]);
+#pragma unroll
+                for (int q = 0; q < WH; ++q)
+                    win[q] = load_masked<DT, NP>(xs + (size_t)q * p.row_bytes, ms[q]);
             }
             uint8_t *yp = p.y + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
             auto row = [&](int r) {
-                const Vf<NP> g2 = unpack<DT, NP>(load_raw<NP>(xs + (size_t)(r + 2) * p.row_bytes));
-                const uint32_t keep = 0u - (uint32_t)ms[r + 2];
+                const Vf<NP> xn = unpack<DT, NP>(load_raw<NP>(xs + (size_t)(r + WH) * p.row_bytes));
+                const uint32_t keep = 0u - (uint32_t)ms[r + WH];
                 uint32_t o[NP];
 #pragma unroll
                 for (int e = 0; e < NP; ++e) {
-                    // products of two 16-bit values are exact in fp32; TwoSum of
-                    // the first two, one more add, then the correction
-                    const float2 p0 = mul2(g0.e[e], w0.e[e]);
-                    const float2 p1 = mul2(g1.e[e], w1.e[e]);
-                    const float2 p2 = mul2(g2.e[e], w2.e[e]);
-                    const float2 s = add2(p0, p1);
-                    const float2 bb = sub2(s, p0);
-                    const float2 err = add2(sub2(p0, sub2(s, bb)), sub2(p1, bb));
-                    const float2 t = add2(s, p2);
-                    o[e] = pack2<DT>(add2(t, err)) & keep;  // output mask
+                    // products of two 16-bit values are exact in fp32; a TwoSum
+                    // cascade over the first W-1 keeps every rounding error,
+                    // the last product is added plainly, then the errors
+                    // (W = 3: TwoSum of the first two, one more add, the
+                    // correction)
+                    float2 pk[W];
+#pragma unroll
+                    for (int k = 0; k < W; ++k)
+                        pk[k] = mul2(k < WH ? win[k].e[e] : xn.e[e], wt[k].e[e]);
+                    float2 s = pk[0], err = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int k = 1; k < W - 1; ++k) {
+                        const float2 sn = add2(s, pk[k]);
+                        const float2 bb = sub2(sn, s);
+                        const float2 ek = add2(sub2(s, sub2(sn, bb)), sub2(pk[k], bb));
+                        err = (k == 1) ? ek : add2(err, ek);
+                        s = sn;
+                    }
+                    float2 t;
+                    if (W >= 3)
+                        t = add2(add2(s, pk[W - 1]), err);
+                    else if (W == 2)
+                        t = add2(s, pk[1]);
+                    else
+                        t = s;
+                    o[e] = pack2<DT>(t) & keep;  // output mask
                 }
                 store_cs<NP>(yp + (int64_t)r * row_stride, o);
-                g0 = g1;
-                g1 = g2;
+#pragma unroll
+                for (int q = 0; q + 1 < WH; ++q)
+                    win[q] = win[q + 1];
+                if (WH > 0)
+                    win[WH > 0 ? WH - 1 : 0] = xn;
             };
             if (n == R) {
 #pragma unroll
@@ -221,9 +247,12 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
     return dead;
 }
 
-template <int DT, int R, int NP>
-__global__ void __launch_bounds__(kFwdMaxThreads) mcc1d_fwd_main(const __grid_constant__ FwdParams p)
+template <int DT, int R, int NP, int W>
+__device__ __forceinline__ void fwd_body(const FwdParams &p)
 {
+    // one producer lane per staged row, and the stage's flag bytes fit the
+    // slot's 32-byte record
+    static_assert(R + W - 1 <= 32, "a stage must not stage more rows than a warp has lanes");
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_err;
     const int c = blockIdx.x;
@@ -244,9 +273,9 @@ __global__ void __launch_bounds__(kFwdMaxThreads) mcc1d_fwd_main(const __grid_co
     const int lane = threadIdx.x & 31;
     bool dead;
     if (threadIdx.x < 32)
-        dead = fwd_produce<R>(p, smem, r0, r1, lane);
+        dead = fwd_produce<R, W>(p, smem, r0, r1, lane);
     else
-        dead = fwd_consume<DT, R, NP>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
+        dead = fwd_consume<DT, R, NP, W>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
     if (dead && lane == 0)
         atomicOr(&s_err, 1);
     __syncthreads();
@@ -254,22 +283,64 @@ __global__ void __launch_bounds__(kFwdMaxThreads) mcc1d_fwd_main(const __grid_co
         atomicOr(p.status, kErrTimeout);
 }
 
+template <int DT, int R, int NP, int W>
+__global__ void __launch_bounds__(kFwdMaxThreads) mcc1d_fwd_main(const __grid_constant__ FwdParams p)
+{
+    fwd_body<DT, R, NP, W>(p);
+}
+
+// The same kernel compiled for one CTA per SM, for the widest kernels, whose
+// W weights and W-1 window rows per channel need the registers.
+template <int DT, int R, int NP, int W>
+__global__ void __launch_bounds__(kFwdMaxThreads, 1) mcc1d_fwd_main_1(const __grid_constant__ FwdParams p)
+{
+    fwd_body<DT, R, NP, W>(p);
+}
+
 typedef void (*FwdFn)(FwdParams);
 
-static FwdFn fwd_kernel(int dtype, int vec)
+// W = 3 (the page's width) with 8 or 4 channels per thread; other widths with
+// 4 (their plan keeps H-blocks of at most 1024 channels), from W = 6 in the
+// one-CTA form.
+template <int DT, int W>
+static FwdFn fwd_pick(int vec)
 {
-    if (dtype == 0)
-        return vec == 4 ? mcc1d_fwd_main<0, kFwdR, 2> : mcc1d_fwd_main<0, kFwdR, 4>;
-    return vec == 4 ? mcc1d_fwd_main<1, kFwdR, 2> : mcc1d_fwd_main<1, kFwdR, 4>;
+    if constexpr (W == 3)
+        return vec == 4 ? mcc1d_fwd_main<DT, kFwdR, 2, 3> : mcc1d_fwd_main<DT, kFwdR, 4, 3>;
+    else if constexpr (W >= 6)
+        return vec == 4 ? mcc1d_fwd_main_1<DT, kFwdR, 2, W> : nullptr;
+    else
+        return vec == 4 ? mcc1d_fwd_main<DT, kFwdR, 2, W> : nullptr;
+}
+
+template <int DT>
+static FwdFn fwd_pick_w(int vec, int W)
+{
+    switch (W) {
+    case 1: return fwd_pick<DT, 1>(vec);
+    case 2: return fwd_pick<DT, 2>(vec);
+    case 3: return fwd_pick<DT, 3>(vec);
+    case 4: return fwd_pick<DT, 4>(vec);
+    case 5: return fwd_pick<DT, 5>(vec);
+    case 6: return fwd_pick<DT, 6>(vec);
+    case 7: return fwd_pick<DT, 7>(vec);
+    case 8: return fwd_pick<DT, 8>(vec);
+    default: return nullptr;
+    }
+}
+
+static FwdFn fwd_kernel(int dtype, int vec, int W)
+{
+    return dtype == 0 ? fwd_pick_w<0>(vec, W) : fwd_pick_w<1>(vec, W);
 }
 
 FwdRing fwd_ring(const Plan &pl)
 {
-    // kFwdR output rows plus the two halo rows per slot; as many slots as the
+    // kFwdR output rows plus the W-1 halo rows per slot; as many slots as the
     // CTA's share of shared memory allows, 2 .. kFwdMaxStages
     FwdRing r;
     r.rows_per_stage = kFwdR;
-    r.slot_bytes = (uint32_t)(kFwdR + 2) * pl.row_bytes;
+    r.slot_bytes = (uint32_t)(kFwdR + pl.W - 1) * pl.row_bytes;
     int64_t budget = kSmemPerSM / pl.ctas_per_sm - kSmemReservedPerCta;
     if (budget > kSmemDynMax)
         budget = kSmemDynMax;
@@ -286,21 +357,26 @@ FwdRing fwd_ring(const Plan &pl)
     return r;
 }
 
-int fwd_kernel_regs(int dtype, int vec)
+int fwd_kernel_regs(int dtype, int vec, int W)
 {
     // registers per thread of the forward instance (cached per device and
     // instance; 0 when the runtime cannot say)
-    static std::atomic<int> cache[64][4];
+    static std::atomic<int> cache[64][4 * (kMaxW + 1)];
+    if (W < 1 || W > kMaxW)
+        return 0;
+    const FwdFn fn = fwd_kernel(dtype, vec, W);
+    if (fn == nullptr)
+        return 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 0;
-    const int slot = dtype * 2 + (vec == 4 ? 1 : 0);
+    const int slot = (dtype * 2 + (vec == 4 ? 1 : 0)) * (kMaxW + 1) + W;
     std::atomic<int> &c = cache[dev & 63][slot];
     int r = c.load(std::memory_order_acquire);
     if (r > 0)
         return r;
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, reinterpret_cast<const void *>(fwd_kernel(dtype, vec))) != cudaSuccess)
+    if (cudaFuncGetAttributes(&a, reinterpret_cast<const void *>(fn)) != cudaSuccess)
         return 0;
     c.store(a.numRegs, std::memory_order_release);
     return a.numRegs;
@@ -332,9 +408,11 @@ int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint
     const uint32_t smem = ring.smem_bytes;
     fp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && !long_ranges(pl)) ? 1 : 0;
 
-    FwdFn fn = fwd_kernel(pl.dtype, pl.vec);
-    static std::atomic<uint64_t> done[4];
-    const int slot_id = pl.dtype * 2 + (pl.vec == 4 ? 1 : 0);
+    FwdFn fn = fwd_kernel(pl.dtype, pl.vec, pl.W);
+    if (fn == nullptr)
+        return kErrCuda;
+    static std::atomic<uint64_t> done[4 * (kMaxW + 1)];
+    const int slot_id = (pl.dtype * 2 + (pl.vec == 4 ? 1 : 0)) * (kMaxW + 1) + pl.W;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return kErrCuda;

@@ -48,7 +48,7 @@ FwdRing fwd_ring(const Plan &p);
 int32_t launch_wait_selftest(int32_t *status, int32_t arrive, cudaStream_t stream);
 // Registers per thread of the forward kernel instance for (dtype, vec), from
 // the runtime (0 when unknown).
-int fwd_kernel_regs(int dtype, int vec);
+int fwd_kernel_regs(int dtype, int vec, int W);
 int32_t launch_fwd(const Plan &p, const void *x, const void *weight, const uint8_t *mask, void *y,
                    int32_t *status, cudaStream_t stream);
 

@@ -267,7 +267,9 @@ int32_t mcc1d_bwd_noalloc(const void *gradY, const void *x, const void *weight,
  *                up (it is never cleared: zero it before the call to use it), or NULL
  *
  * Enqueued on `stream`; no workspace; deterministic; y within 1 ulp of the
- * exact value rounded once. Errors and shape limits as mcc1d_bwd.
+ * exact value rounded once. Errors and shape limits as mcc1d_bwd, except the
+ * kernel width: any 1 <= W <= 8 (the page's W = 3, and the widths the strided
+ * backward accepts, so a caller gets both directions of the same conv).
  */
 int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *mask_or_null, void *y,
                   void *stream, int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
@@ -279,7 +281,7 @@ int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *mask_or_null
  * per thread, warps, rows per stage, ring depth, CTAs, shared memory,
  * workspace layout, reduce shape; per-H-block CTA and slot ranges as comma
  * lists). kind: MCC1D_PLAN_BWD (mcc1d_bwd, W = 3), MCC1D_PLAN_BWD_EX (the
- * strided calls, 1 <= W <= 8) or MCC1D_PLAN_FWD (mcc1d_fwd; with a GPU the
+ * strided calls, 1 <= W <= 8) or MCC1D_PLAN_FWD (mcc1d_fwd, 1 <= W <= 8; with a GPU the
  * forward's plan also depends on its kernel's register count). Writes at most
  * buf_bytes - 1 characters plus a terminating NUL to buf (buf may be NULL);
  * *needed_out (optional) receives the full length + 1. Host only; shape

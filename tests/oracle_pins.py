@@ -326,7 +326,8 @@ def pin_forward_torch(orc):
     torch's float64 conv1d (left padding W-1, groups = H) on the CPU."""
     rng = np.random.default_rng(41)
     for dt in ("bf16", "fp16"):
-        for (S, B, H, W) in ((1, 2, 3, 3), (6, 2, 5, 3), (40, 3, 7, 3), (9, 1, 4, 5)):
+        for (S, B, H, W) in ((1, 2, 3, 3), (6, 2, 5, 3), (40, 3, 7, 3), (9, 1, 4, 5), (17, 2, 6, 1),
+                             (17, 2, 6, 2), (17, 2, 6, 4), (17, 2, 6, 8), (3, 2, 4, 7)):
             x, w = rand_bits(rng, (S, B, H), dt), rand_bits(rng, (W, H), dt)
             mask = (rng.random((B, S)) < 0.7).astype(np.uint8)
             y = orc.fwd(S, B, H, W, dt, x, w, mask)

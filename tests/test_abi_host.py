@@ -176,7 +176,7 @@ def test_fwd_rejects_before_any_launch(lib):
     assert call(x=None) == NULLPTR and call(y=None) == NULLPTR and call(w=None) == NULLPTR
     assert call(x=0x1008) == INVALID and call(y=0x3002) == INVALID
     assert call(dt=2) == INVALID
-    assert call(B=0) == SHAPE and call(H=4000) == SHAPE and call(W=5) == SHAPE
+    assert call(B=0) == SHAPE and call(H=4000) == SHAPE and call(W=0) == SHAPE and call(W=9) == SHAPE
 
 
 def test_ex_accepts_widths_one_to_eight(lib):

@@ -1,9 +1,10 @@
 """The forward kernel (mcc1d_fwd) against the oracle's forward.
 
-y(t,j,h) = mask(j,t) * sum_k weight(k,h) * x(t-2+k, j, h), x zero before
+y(t,j,h) = mask(j,t) * sum_k weight(k,h) * x(t-(W-1)+k, j, h), x zero before
 t = 0: the map whose transpose is the page's backward. y must be within
 1 ulp of the oracle's fp64 value rounded once, at full workload sizes and on
-edge shapes; masked rows are exactly zero.
+edge shapes, for W = 3 and every other width 1..8; masked rows are exactly
+zero.
 """
 import numpy as np
 import pytest
@@ -26,7 +27,7 @@ def cuda_ready():
     build.build()
 
 
-def run_fwd(inp, S, B, H, dt, mask_override=None, use_override=False):
+def run_fwd(inp, S, B, H, dt, mask_override=None, use_override=False, W=3):
     x = to_device(inp["x"], dt)
     w = to_device(inp["w"], dt)
     mask = mask_override if use_override else inp["mask"]
@@ -34,7 +35,7 @@ def run_fwd(inp, S, B, H, dt, mask_override=None, use_override=False):
     y = torch.empty_like(x)
     y.view(torch.int16).fill_(-1)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    m.mcc1d_fwd(x, w, md, y, torch.cuda.current_stream(), S, B, H, 3, dt, status)
+    m.mcc1d_fwd(x, w, md, y, torch.cuda.current_stream(), S, B, H, W, dt, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return y.view(torch.int16).cpu().numpy().view(np.uint16)
@@ -95,3 +96,29 @@ def test_forward_deterministic():
     a = run_fwd(inp, wl.S, wl.B, wl.H, wl.dtype)
     for _ in range(3):
         assert np.array_equal(a, run_fwd(inp, wl.S, wl.B, wl.H, wl.dtype))
+
+
+WIDTHS = []
+for W in (1, 2, 4, 5, 6, 7, 8):
+    for (S, B, H, dt) in ((1, 2, 384, "bf16"), (W, 1, 1088, "fp16"), (W + 1, 3, 448, "bf16"),
+                          (77, 3, 2112, "fp16"), (5000, 2, 640, "bf16")):
+        WIDTHS.append((W, S, B, H, dt))
+
+
+@pytest.mark.parametrize("W,S,B,H,dt", WIDTHS, ids=[f"w{a}_s{b}_b{c}_h{d}_{e}" for a, b, c, d, e in WIDTHS])
+def test_forward_widths(W, S, B, H, dt):
+    wl = datagen.Workload("fw", S, B, H, dt, W=W, mask=("bernoulli", 0.8))
+    inp = datagen.generate(wl, seed=W * 31 + S)
+    y = run_fwd(inp, S, B, H, dt, W=W)
+    ref = oracle.fwd_bits(S, B, H, W, dt, inp["x"], inp["w"], inp["mask"])
+    assert max_ulp(y, ref) <= GX_MAX_ULP
+
+
+@pytest.mark.parametrize("W", [2, 4, 8])
+def test_forward_width_full_size(W):
+    """4096 x 8 x 2048 bf16 (a full workload) at other widths."""
+    wl = datagen.WORKLOADS["s4096_b8_h2048_bf16"].resized(W=W)
+    inp = datagen.generate(wl, seed=W)
+    y = run_fwd(inp, wl.S, wl.B, wl.H, wl.dtype, W=W)
+    ref = oracle.fwd_bits(wl.S, wl.B, wl.H, W, wl.dtype, inp["x"], inp["w"], inp["mask"])
+    assert max_ulp(y, ref) <= GX_MAX_ULP

@@ -92,10 +92,11 @@ def check_bwd(p, S, B, H, W):
     assert p["reduce_blocks"] == p["n_hb"] * W * cdiv(p["hb_width"], 4 * p["red_lanes"])
 
 
-def check_fwd(p, S, B, H):
-    check_common(p, S, B, H, 3)
-    assert p["rows_per_stage"] + 2 <= 32
-    assert p["slot_bytes"] == (p["rows_per_stage"] + 2) * p["row_bytes"]
+def check_fwd(p, S, B, H, W=3):
+    check_common(p, S, B, H, W)
+    assert p["rows_per_stage"] + W - 1 <= 32       # one producer lane per staged row
+    assert p["slot_bytes"] == (p["rows_per_stage"] + W - 1) * p["row_bytes"]
+    assert W == 3 or (p["hb_width"] <= 1024 and p["vec"] == 4)
     assert p["ws_bytes"] == 0
 
 
@@ -134,9 +135,10 @@ def test_strided_plans_every_width(W):
         check_bwd(p, S, B, H, W)
 
 
-def test_forward_plans():
-    for (S, B, H) in SHAPES[::2]:
-        check_fwd(m.mcc1d_plan_describe(S, B, H, 3, "bf16", m.PLAN_FWD), S, B, H)
+@pytest.mark.parametrize("W", range(1, 9))
+def test_forward_plans(W):
+    for (S, B, H) in SHAPES[:: 2 if W == 3 else 5]:
+        check_fwd(m.mcc1d_plan_describe(S, B, H, W, "bf16", m.PLAN_FWD), S, B, H, W)
 
 
 def test_bench_workload_plan():
@@ -151,5 +153,7 @@ def test_describe_rejects():
         m.mcc1d_plan_describe(64, 2, 384, 4, "bf16", m.PLAN_BWD)      # page calls: W = 3
     with pytest.raises(m.Mcc1dError):
         m.mcc1d_plan_describe(64, 2, 384, 9, "bf16", m.PLAN_BWD_EX)
+    with pytest.raises(m.Mcc1dError):
+        m.mcc1d_plan_describe(64, 2, 384, 9, "bf16", m.PLAN_FWD)
     with pytest.raises(m.Mcc1dError):
         m.mcc1d_plan_describe(64, 2, 384, 3, "bf16", 7)
