@@ -32,6 +32,14 @@ class Mcc1dTensors(ctypes.Structure):
                 ("gradX", ctypes.c_void_p), ("gradWeight", ctypes.c_void_p)]
 
 
+class Mcc1dFwdTensors(ctypes.Structure):
+    """Mirror of ``mcc1d_fwd_tensors`` (the forward's strided inputs)."""
+    _fields_ = [("x", ctypes.c_void_p), ("x_strides", ctypes.c_int64 * 3),
+                ("weight", ctypes.c_void_p), ("weight_strides", ctypes.c_int64 * 2),
+                ("mask", ctypes.c_void_p), ("mask_strides", ctypes.c_int64 * 2),
+                ("y", ctypes.c_void_p)]
+
+
 class Mcc1dError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
@@ -78,6 +86,11 @@ def load():
         lib.mcc1d_plan_describe.argtypes = [i64, i64, i64, i64, i32, i32, ctypes.c_char_p, u64,
                                             ctypes.POINTER(u64)]
         lib.mcc1d_plan_describe.restype = i32
+        lib.mcc1d_fwd_ex_workspace_size.argtypes = [ctypes.POINTER(Mcc1dFwdTensors), i64, i64, i64, i64,
+                                                    i32, ctypes.POINTER(u64)]
+        lib.mcc1d_fwd_ex_workspace_size.restype = i32
+        lib.mcc1d_fwd_ex.argtypes = [ctypes.POINTER(Mcc1dFwdTensors), i64, i64, i64, i64, i32, vp, u64, vp, vp]
+        lib.mcc1d_fwd_ex.restype = i32
         lib.mcc1d_selftest_wait.argtypes = [vp, i32, vp]
         lib.mcc1d_selftest_wait.restype = i32
         _lib = lib
@@ -135,6 +148,37 @@ def tensors(gradY, x, weight, mask, gradX, gradWeight) -> Mcc1dTensors:
     return t
 
 
+def fwd_tensors(x, weight, mask, y) -> Mcc1dFwdTensors:
+    """Forward descriptor of torch tensors (data pointers and element strides)."""
+    t = Mcc1dFwdTensors()
+    t.x, t.weight, t.y = x.data_ptr(), weight.data_ptr(), y.data_ptr()
+    t.x_strides[:] = list(x.stride())
+    t.weight_strides[:] = list(weight.stride())
+    if mask is not None:
+        t.mask = mask.data_ptr()
+        t.mask_strides[:] = [st * mask.element_size() for st in mask.stride()]
+    return t
+
+
+def mcc1d_fwd_ex_workspace_size(t: Mcc1dFwdTensors, S, B, H, W, dtype) -> int:
+    v = ctypes.c_uint64(0)
+    st = load().mcc1d_fwd_ex_workspace_size(ctypes.byref(t), S, B, H, W, dtype_code(dtype), ctypes.byref(v))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_fwd_ex_workspace_size")
+    return int(v.value)
+
+
+def mcc1d_fwd_ex(t: Mcc1dFwdTensors, S, B, H, W, dtype, workspace, workspace_bytes, stream,
+                 device_status=None) -> None:
+    """Enqueue the forward on strided tensors described by ``t``."""
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = load().mcc1d_fwd_ex(ctypes.byref(t), S, B, H, W, dtype_code(dtype), _ptr(workspace),
+                             int(workspace_bytes), stream or None, _ptr(device_status))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_fwd_ex")
+
+
 def mcc1d_bwd_ex_workspace_size(t: Mcc1dTensors, S, B, H, W, dtype) -> int:
     out = ctypes.c_uint64(0)
     st = load().mcc1d_bwd_ex_workspace_size(ctypes.byref(t), S, B, H, W, dtype_code(dtype),
@@ -178,16 +222,26 @@ def mcc1d_fwd(x, weight, mask_or_null, y, stream, S, B, H, W, dtype, device_stat
 
 
 def forward(x, weight, mask=None, *, y=None, stream=None):
-    """Convenience forward on dense torch CUDA tensors; returns y."""
+    """Convenience forward on torch CUDA tensors x [S,B,H], weight [W,H]
+    (1 <= W <= 8), mask [B,S] or None; inputs may be strided views (they go
+    through mcc1d_fwd_ex). Returns y (dense; allocated when not given)."""
     import torch
     S, B, H = x.shape
+    W = weight.shape[0]
     if mask is not None and mask.dtype == torch.bool:
         mask = mask.view(torch.uint8)
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty((S, B, H), dtype=x.dtype, device=x.device)
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
-    mcc1d_fwd(x, weight, mask, y, stream, S, B, H, weight.shape[0], dtype_code(x.dtype))
+    dense = x.is_contiguous() and weight.is_contiguous() and (mask is None or mask.is_contiguous())
+    if dense:
+        mcc1d_fwd(x, weight, mask, y, stream, S, B, H, W, dtype_code(x.dtype))
+    else:
+        t = fwd_tensors(x, weight, mask, y)
+        nb = mcc1d_fwd_ex_workspace_size(t, S, B, H, W, x.dtype)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=x.device)
+        mcc1d_fwd_ex(t, S, B, H, W, x.dtype, ws, nb, stream)
     return y
 
 

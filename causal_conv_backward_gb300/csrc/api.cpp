@@ -257,8 +257,102 @@ extern "C" int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *m
     st = fwd_plan(S, B, H, W, dtype, &p);
     if (st != kOk)
         return st;
-    return launch_fwd(p, x, weight, mask_or_null, y, device_status_or_null,
+    return launch_fwd(p, dense_layout(S, B, H), x, weight, mask_or_null, y, device_status_or_null,
                       static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+// Plan of a strided forward: whether x is gathered into the workspace first.
+struct FwdExPlan {
+    Layout L;          // layout the kernel reads (dense x when gathered)
+    Layout in;         // the caller's layout
+    bool pack_x;
+    uint64_t bytes;
+};
+
+// Validation and layout of a strided forward call (no device work).
+int32_t make_fwd_ex(const mcc1d_fwd_tensors *t, int64_t S, int64_t B, int64_t H, int64_t W,
+                    int32_t dtype, FwdExPlan *e)
+{
+    if (!t || !t->x || !t->weight || !t->y)
+        return kErrNull;
+    const int32_t st = validate_shape_w(S, B, H, W, dtype);
+    if (st != kOk)
+        return st;
+    Layout in = dense_layout(S, B, H);
+    const int64_t dims3[3] = {S, B, H};
+    for (int d = 0; d < 3; ++d) {
+        if (t->x_strides[d] < 0)
+            return kErrInvalid;
+        in.x[d] = dims3[d] == 1 ? 0 : t->x_strides[d];
+    }
+    const int64_t dimsw[2] = {W, H}, dimsm[2] = {B, S};
+    for (int d = 0; d < 2; ++d) {
+        if (t->weight_strides[d] < 0 || (t->mask && t->mask_strides[d] < 0))
+            return kErrInvalid;
+        in.w[d] = dimsw[d] == 1 ? 0 : t->weight_strides[d];
+        in.m[d] = dimsm[d] == 1 ? 0 : t->mask_strides[d];
+    }
+    if (((uintptr_t)t->x & 1u) || ((uintptr_t)t->weight & 1u) || !aligned16(t->y))
+        return kErrInvalid;
+    e->in = in;
+    e->L = in;
+    e->pack_x = !streamable(t->x, in.x);
+    e->bytes = 0;
+    if (e->pack_x) {
+        const Layout dense = dense_layout(S, B, H);
+        for (int d = 0; d < 3; ++d)
+            e->L.x[d] = dense.x[d];
+        e->bytes = round256((uint64_t)S * (uint64_t)B * (uint64_t)H * 2u);
+    }
+    return kOk;
+}
+
+}  // namespace
+
+extern "C" int32_t mcc1d_fwd_ex_workspace_size(const mcc1d_fwd_tensors *t, int64_t S, int64_t B,
+                                               int64_t H, int64_t W, int32_t dtype,
+                                               uint64_t *bytes_out)
+{
+    if (!bytes_out)
+        return kErrNull;
+    FwdExPlan e;
+    const int32_t st = make_fwd_ex(t, S, B, H, W, dtype, &e);
+    if (st != kOk)
+        return st;
+    *bytes_out = e.bytes;
+    return kOk;
+}
+
+extern "C" int32_t mcc1d_fwd_ex(const mcc1d_fwd_tensors *t, int64_t S, int64_t B, int64_t H, int64_t W,
+                                int32_t dtype, void *workspace, uint64_t workspace_bytes, void *stream,
+                                int32_t *device_status_or_null)
+{
+    FwdExPlan e;
+    int32_t st = make_fwd_ex(t, S, B, H, W, dtype, &e);
+    if (st != kOk)
+        return st;
+    if (e.bytes > 0) {
+        if (!workspace)
+            return kErrNull;
+        if (!aligned16(workspace))
+            return kErrInvalid;
+        if (workspace_bytes < e.bytes)
+            return kErrWorkspace;
+    }
+    Plan p;
+    st = fwd_plan(S, B, H, W, dtype, &p);
+    if (st != kOk)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const void *x = t->x;
+    if (e.pack_x) {
+        if (launch_pack(t->x, e.in.x, workspace, S, B, H, s) != kOk)
+            return kErrCuda;
+        x = workspace;
+    }
+    return launch_fwd(p, e.L, x, t->weight, t->mask, t->y, device_status_or_null, s);
 }
 
 extern "C" int32_t mcc1d_plan_describe(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,

@@ -42,6 +42,10 @@ struct FwdParams {
     int32_t B, hb_width, ncta, stages;
     uint32_t row_bytes, slot_bytes, off_mask, off_bar;
     int32_t contig_rows;
+    // Input strides (elements; mask bytes); x has unit H stride and 16-byte
+    // aligned rows (other layouts are gathered into a dense copy first).
+    int64_t x_s, x_b, w_k, w_h, m_b, m_s;
+    int32_t w_vec;         // weight rows can be read as aligned vectors
 };
 
 // Byte q of a stage (row cursor at output row t = c.i): q < W-1 says whether
@@ -59,7 +63,7 @@ __device__ __forceinline__ uint32_t fwd_stage_byte(const FwdParams &p, const Cur
         return 0;
     if (p.mask == nullptr)
         return 1;
-    return __ldg(p.mask + (int64_t)c.j * p.S + row) != 0 ? 1u : 0u;
+    return __ldg(p.mask + (int64_t)c.j * p.m_b + row * p.m_s) != 0 ? 1u : 0u;
 }
 
 template <int R, int W>
@@ -69,7 +73,6 @@ __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64
     const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
     const uint32_t ring0 = smem_u32(smem);
-    const int64_t row_elems = (int64_t)p.B * p.H;
     Cursor cur;
     cur.init(r0, r1, p.S, p.BS);
     int slot = 0, stage = 0;
@@ -109,11 +112,11 @@ __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64
         const uint32_t slot_base = ring0 + (uint32_t)slot * p.slot_bytes;
         if (p.contig_rows) {
             if (lane == 0)
-                bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.x + 2 * (cur.i - (W - 1) + q0) * p.H,
+                bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.x + 2 * (cur.i - (W - 1) + q0) * p.x_s,
                          (uint32_t)nrows * wbytes, bar_full0 + 8u * slot);
         } else if (lane < nrows) {
             const int q = q0 + lane;
-            const int64_t e = (cur.i - (W - 1) + q) * row_elems + (int64_t)cur.j * p.H + hb0;
+            const int64_t e = (cur.i - (W - 1) + q) * p.x_s + (int64_t)cur.j * p.x_b + hb0;
             bulk_g2s(slot_base + (uint32_t)q * p.row_bytes, p.x + 2 * e, wbytes, bar_full0 + 8u * slot);
         }
         cur.advance(n, p.S, p.B);
@@ -130,6 +133,23 @@ __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             dead = true;
     }
     return __any_sync(0xFFFFFFFFu, dead);
+}
+
+// Weight row k for channels h .. h + 2*NP - 1: one vector load when the rows
+// are dense and aligned, else one 16-bit load per channel.
+template <int DT, int NP>
+__device__ __forceinline__ Vf<NP> fwd_weight(const FwdParams &p, int k, int64_t h)
+{
+    if (p.w_vec)
+        return unpack<DT, NP>(ldg_raw<NP>(p.w + k * p.w_k + h));
+    Raw<NP> r;
+#pragma unroll
+    for (int e = 0; e < NP; ++e) {
+        const uint32_t lo = __ldg(p.w + k * p.w_k + (h + 2 * e) * p.w_h);
+        const uint32_t hi = __ldg(p.w + k * p.w_k + (h + 2 * e + 1) * p.w_h);
+        r.u[e] = lo | (hi << 16);
+    }
+    return unpack<DT, NP>(r);
 }
 
 template <int DT, int R, int NP, int W>
@@ -166,7 +186,7 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             if (active) {
 #pragma unroll
                 for (int k = 0; k < W; ++k)
-                    wt[k] = unpack<DT, NP>(ldg_raw<NP>(p.w + k * p.H + hb0 + CH * ct));
+                    wt[k] = fwd_weight<DT, NP>(p, k, hb0 + CH * ct);
             }
         }
         if (!dead) {
@@ -382,8 +402,8 @@ int fwd_kernel_regs(int dtype, int vec, int W)
     return a.numRegs;
 }
 
-int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint8_t *mask, void *y,
-                   int32_t *status, cudaStream_t stream)
+int32_t launch_fwd(const Plan &pl, const Layout &L, const void *x, const void *weight, const uint8_t *mask,
+                   void *y, int32_t *status, cudaStream_t stream)
 {
     // Same CTA partition as the backward; the ring holds x rows only.
     FwdParams fp;
@@ -406,7 +426,14 @@ int32_t launch_fwd(const Plan &pl, const void *x, const void *weight, const uint
     fp.off_mask = ring.off_mask;
     fp.off_bar = ring.off_bar;
     const uint32_t smem = ring.smem_bytes;
-    fp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && !long_ranges(pl)) ? 1 : 0;
+    fp.x_s = L.x[0];
+    fp.x_b = L.x[1];
+    fp.w_k = L.w[0];
+    fp.w_h = L.w[1];
+    fp.m_b = L.m[0];
+    fp.m_s = L.m[1];
+    fp.w_vec = (L.w[1] == 1 && (L.w[0] * 2) % 16 == 0 && ((uintptr_t)weight & 15u) == 0) ? 1 : 0;
+    fp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && L.x[0] == pl.H && !long_ranges(pl)) ? 1 : 0;
 
     FwdFn fn = fwd_kernel(pl.dtype, pl.vec, pl.W);
     if (fn == nullptr)

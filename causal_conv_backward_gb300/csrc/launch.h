@@ -33,8 +33,6 @@ int32_t launch_direct(const Plan &p, const void *gradY, const void *x, const voi
 int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_t S, int64_t B,
                     int64_t H, cudaStream_t stream);
 
-// Enqueues the forward kernel of plan `p` (dense tensors). `status` is a
-// device word the kernel ORs kErrTimeout into if a wait gives up, or null.
 // The forward's shared-memory ring for plan `p` (its own rows per stage and
 // depth; the backward's ring fields of the plan do not apply to it).
 struct FwdRing {
@@ -46,10 +44,13 @@ FwdRing fwd_ring(const Plan &p);
 // kOk (arrive != 0: it arrives first) or kErrTimeout (nothing arrives) to the
 // device word `status`.
 int32_t launch_wait_selftest(int32_t *status, int32_t arrive, cudaStream_t stream);
-// Registers per thread of the forward kernel instance for (dtype, vec), from
-// the runtime (0 when unknown).
+// Registers per thread of the forward kernel instance for (dtype, vec, W),
+// from the runtime (0 when unknown).
 int fwd_kernel_regs(int dtype, int vec, int W);
-int32_t launch_fwd(const Plan &p, const void *x, const void *weight, const uint8_t *mask, void *y,
-                   int32_t *status, cudaStream_t stream);
+// Enqueues the forward kernel of plan `p`; the inputs are read with layout L
+// (x with unit H stride and 16-byte aligned rows), y is dense. `status` is a
+// device word the kernel ORs kErrTimeout into if a wait gives up, or null.
+int32_t launch_fwd(const Plan &p, const Layout &L, const void *x, const void *weight, const uint8_t *mask,
+                   void *y, int32_t *status, cudaStream_t stream);
 
 }  // namespace mcc1d

@@ -276,6 +276,45 @@ int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *mask_or_null
                   int32_t *device_status_or_null);
 
 /*
+ * The forward on strided inputs, as mcc1d_bwd_ex is the backward's: strides
+ * in elements (bytes for the mask), outermost first, negative strides
+ * rejected, strides of size-1 dimensions ignored.
+ *
+ *   x       [S,B,H] input: strides {S, B, H}; 2-byte aligned
+ *   weight  [W,H]   input: strides {W, H}; 2-byte aligned; read in place
+ *   mask    [B,S]   input bytes or NULL: strides {B, S}; read in place
+ *   y       [S,B,H] output, dense (strides {B*H, H, 1}), 16-byte aligned
+ *
+ * x with unit H stride and 16-byte aligned rows (base and the S and B
+ * strides in bytes multiples of 16) is streamed in place and the call needs
+ * no workspace (size 0; workspace may be NULL). Any other x is first gathered
+ * into a dense copy in the workspace: S*B*H*2 bytes rounded up to 256. y is
+ * bitwise identical to mcc1d_fwd's on a dense copy of the same values.
+ */
+typedef struct mcc1d_fwd_tensors {
+    const void *x;
+    int64_t x_strides[3];
+    const void *weight;
+    int64_t weight_strides[2];
+    const uint8_t *mask;
+    int64_t mask_strides[2];
+    void *y;
+} mcc1d_fwd_tensors;
+
+/* Workspace bytes of mcc1d_fwd_ex for these tensors (0 when x streams in
+ * place). Validation as mcc1d_fwd (1 <= W <= 8) plus the stride and
+ * alignment rules above. Host only. */
+int32_t mcc1d_fwd_ex_workspace_size(const mcc1d_fwd_tensors *t, int64_t S, int64_t B, int64_t H,
+                                    int64_t W, int32_t dtype, uint64_t *bytes_out);
+
+/* Enqueue the forward on the tensors described by `t` (see above); errors as
+ * mcc1d_fwd_ex_workspace_size and mcc1d_fwd, MCC1D_ERR_WORKSPACE if a needed
+ * workspace is smaller than mcc1d_fwd_ex_workspace_size. */
+int32_t mcc1d_fwd_ex(const mcc1d_fwd_tensors *t, int64_t S, int64_t B, int64_t H, int64_t W,
+                     int32_t dtype, void *workspace, uint64_t workspace_bytes, void *stream,
+                     int32_t *device_status_or_null);
+
+/*
  * Diagnostics (no counterpart on the page): the execution plan the library
  * would use for a shape, as text lines "key=value" (H-block split, channels
  * per thread, warps, rows per stage, ring depth, CTAs, shared memory,

@@ -191,3 +191,52 @@ def test_ex_accepts_widths_one_to_eight(lib):
     assert ex_size(desc(), W=0)[0] == SHAPE
     assert ex_size(desc(), W=9)[0] == SHAPE
     assert ws(64, 2, 384, W=4)[0] == SHAPE   # page call: W must be 3
+
+
+# ------------------------------------------------------- strided forward calls
+def fdesc(x=0x20000, w=0x30000, mask=None, y=0x40000, xs=None, ws_=None, ms=None, S=64, B=2, H=384):
+    t = m.Mcc1dFwdTensors()
+    t.x, t.weight, t.mask, t.y = x, w, mask, y
+    t.x_strides[:] = xs or [B * H, H, 1]
+    t.weight_strides[:] = ws_ or [H, 1]
+    t.mask_strides[:] = ms or [S, 1]
+    return t
+
+
+def fex_size(t, S=64, B=2, H=384, W=3, dt=0):
+    v = ctypes.c_uint64(7)
+    st = m.load().mcc1d_fwd_ex_workspace_size(ctypes.byref(t), S, B, H, W, dt, ctypes.byref(v))
+    return st, v.value
+
+
+def test_fwd_ex_workspace_sizes(lib):
+    S, B, H = 64, 2, 384
+    assert fex_size(fdesc()) == (0, 0)                                   # dense: streamed in place
+    assert fex_size(fdesc(xs=[H, S * H, 1])) == (0, 0)                   # [B,S,H] memory: in place
+    n = S * B * H * 2
+    assert fex_size(fdesc(xs=[B * 2 * H, 2 * H, 2])) == (0, (n + 255) // 256 * 256)   # gathered
+    assert fex_size(fdesc(x=0x20002)) == (0, (n + 255) // 256 * 256)    # rows off 16 B: gathered
+    for W in range(1, 9):
+        assert fex_size(fdesc(ws_=[H, 1]), W=W)[0] == 0
+
+
+def test_fwd_ex_rejects_before_any_launch(lib):
+    assert fex_size(fdesc(x=None))[0] == NULLPTR
+    assert fex_size(fdesc(y=None))[0] == NULLPTR
+    assert fex_size(fdesc(w=None))[0] == NULLPTR
+    assert fex_size(fdesc(xs=[-768, 384, 1]))[0] == INVALID
+    assert fex_size(fdesc(ws_=[384, -1]))[0] == INVALID
+    assert fex_size(fdesc(mask=0x50000, ms=[-64, 1]))[0] == INVALID
+    assert fex_size(fdesc(x=0x20001))[0] == INVALID                     # not 2-byte aligned
+    assert fex_size(fdesc(y=0x40008))[0] == INVALID                     # output not 16-byte aligned
+    assert fex_size(fdesc(), W=9)[0] == SHAPE and fex_size(fdesc(), W=0)[0] == SHAPE
+    assert fex_size(fdesc(), dt=2)[0] == INVALID
+    v = ctypes.c_uint64(0)
+    assert m.load().mcc1d_fwd_ex_workspace_size(None, 64, 2, 384, 3, 0, ctypes.byref(v)) == NULLPTR
+    assert m.load().mcc1d_fwd_ex_workspace_size(ctypes.byref(fdesc()), 64, 2, 384, 3, 0, None) == NULLPTR
+    # a gathered x needs the workspace: missing or small is refused before any device work
+    t = fdesc(xs=[2 * 2 * 384, 2 * 384, 2])
+    f = m.load().mcc1d_fwd_ex
+    assert f(ctypes.byref(t), 64, 2, 384, 3, 0, None, 0, None, None) == NULLPTR
+    assert f(ctypes.byref(t), 64, 2, 384, 3, 0, 0x60000, 1024, None, None) == WORKSPACE
+    assert f(ctypes.byref(t), 64, 2, 384, 3, 0, 0x60008, 1 << 20, None, None) == INVALID
