@@ -1,5 +1,5 @@
 /*
- * mcc1d.h - masked causal depthwise conv1d backward (W = 3) for NVIDIA GB300.
+ * mcc1d.h - masked causal depthwise conv1d backward (and forward) for NVIDIA GB300.
  *
  * C ABI of libmcc1d.so. The operation is the one defined on the CANN operator
  * page "aclnnMaskedCausalConv1dBackward", section 功能说明 (function
@@ -11,7 +11,9 @@
  *   gradWeight(k,h)    = sum over j < B, i < S of gradYMasked(i+W-1-k,j,h) * x(i,j,h)
  *
  * Terms whose S index falls outside [0,S) are zero; batches never mix; H is
- * the depthwise (elementwise) axis. W is 3, the only width the page supports.
+ * the depthwise (elementwise) axis. W is 3 on the page-shaped calls, the only
+ * width the page supports; the strided calls (mcc1d_bwd_ex, mcc1d_fwd_ex) and
+ * the forward take any 1 <= W <= 8 with the same formulas.
  *
  * The page's two-phase call (函数原型 / function prototypes) maps to
  *   1. mcc1d_bwd_workspace_size: validate and size the workspace (host only);
@@ -23,7 +25,9 @@
  *  - Tensor pointers are DEVICE pointers owned by the caller; the library
  *    allocates no memory and keeps no state between calls.
  *  - Tensors are dense and row-major: gradY, x, gradX [S,B,H]; weight and
- *    gradWeight [W,H]; mask [B,S] with one byte per position, nonzero = keep.
+ *    gradWeight [W,H]; mask [B,S] with one byte per position, nonzero = keep
+ *    (the _ex calls take strided inputs through a descriptor; their outputs
+ *    stay dense).
  *  - gradY, x, weight, gradX, gradWeight and workspace must be 16-byte
  *    aligned; the mask may have any alignment.
  *  - The data type (bf16 or fp16) is the same for all five 16-bit tensors, as
@@ -39,7 +43,8 @@
  *    codes >= 561003 are this library's own.
  *
  * Shape limits (约束说明 / constraints): 1 <= B <= 32, 1 <= B*S <= 524288,
- * 384 <= H <= 24576 with H % 64 == 0, W == 3. Anything else is
+ * 384 <= H <= 24576 with H % 64 == 0, W == 3 (1 <= W <= 8 where stated
+ * above). Anything else is
  * MCC1D_ERR_INNER_TILING_ERROR. The page also promises that inputs hold no
  * inf or NaN and that no intermediate value overflows the 16-bit type; the
  * library relies on that and does not check it.
