@@ -24,7 +24,8 @@ def declared_functions():
     names = []
     for f in os.listdir(os.path.join(ROOT, "include")):
         if f.endswith(".h"):
-            src = open(os.path.join(ROOT, "include", f)).read()
+            with open(os.path.join(ROOT, "include", f)) as fh:
+                src = fh.read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
             names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(mcc1d_\w+)\s*\(", src, flags=re.M)
     return sorted(set(names))
