@@ -82,7 +82,8 @@ def pin_golden(orc):
     files = sorted(glob.glob(os.path.join(GOLDEN, "*.json")))
     assert files, "no golden fixtures found"
     for f in files:
-        g = json.load(open(f))
+        with open(f) as fh:
+            g = json.load(fh)
         S, B, H, W, dt = g["S"], g["B"], g["H"], g["W"], g["dtype"]
         if g.get("inputs") == {"gradY": "zeros", "x": "zeros", "weight": "zeros", "mask": "zeros"}:
             gy = np.zeros((S, B, H), np.uint16)

@@ -41,7 +41,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks_aggregate_max_time_and_total_bytes():
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()   # no fork of this (threaded) process
     out = manager.dict()
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     assert out[0] == out[1] == (2.0, 300.0)

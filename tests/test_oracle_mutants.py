@@ -50,7 +50,8 @@ MUTANTS = {
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
-    src = open(oracle.SOURCE).read()
+    with open(oracle.SOURCE) as fh:
+        src = fh.read()
     assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
     mpath = tmp_path / "mutant.c"
     mpath.write_text(src.replace(old, new))
