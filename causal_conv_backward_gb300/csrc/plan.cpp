@@ -79,7 +79,7 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     p->hb_width = (int32_t)round_up(ceil_div(H, p->n_hb), 64);
     // Channels per consumer thread: 8 (16-byte vectors), or 4 (8-byte) within
     // o.vec4_max_warps consumer warps, either always (the forward: twice the
-    // threads in flight per row, at 69 registers against 96; H-blocks up to
+    // threads in flight per row, at about 70 registers against 96; H-blocks up to
     // 1024) or when that leaves a smaller share of the consumer lanes idle
     // (the backward, within 5 warps: H-blocks of 384, 576 and 640; wider
     // blocks would give up their second CTA per SM, which costs more than the
