@@ -408,6 +408,27 @@ def pin_gradx_at(orc):
         assert np.array_equal(bits, r["gx"].ravel()[idx]), dt
 
 
+def pin_thread_independence(orc):
+    """The oracle's results (fp64 sums, their roundings, sum|terms|) are the
+    same bits on one thread and on every thread: each output is one thread's
+    sum in a fixed order, so the parallel runs used at full size are the
+    definition, not an approximation of it."""
+    rng = np.random.default_rng(37)
+    many = orc.threads(0)
+    for dt in ("bf16", "fp16"):
+        for (S, B, H, W) in ((300, 3, 64, 3), (129, 2, 128, 5), (1000, 1, 64, 1)):
+            gy, x = rand_bits(rng, (S, B, H), dt), rand_bits(rng, (S, B, H), dt)
+            w = rand_bits(rng, (W, H), dt)
+            mask = (rng.random((B, S)) < 0.8).astype(np.uint8)
+            one = orc.bwd(S, B, H, W, dt, gy, x, w, mask, want_exact=True, nthreads=1)
+            all_ = orc.bwd(S, B, H, W, dt, gy, x, w, mask, want_exact=True, nthreads=many)
+            for k in one:
+                assert np.array_equal(one[k], all_[k]), (dt, S, B, H, W, k)
+            assert np.array_equal(orc.fwd_bits(S, B, H, W, dt, x, w, mask, nthreads=1),
+                                  orc.fwd_bits(S, B, H, W, dt, x, w, mask, nthreads=many))
+
+
 ALL_PINS = [pin_golden, pin_closed_form_ones, pin_shift_identities, pin_mask_special_cases,
             pin_s1, pin_batch_independence, pin_jacobian_bruteforce, pin_adjoint_identity,
-            pin_torch_autograd, pin_forward_torch, pin_forward_rounding, pin_converters, pin_gradx_at]
+            pin_torch_autograd, pin_forward_torch, pin_forward_rounding, pin_converters, pin_gradx_at,
+            pin_thread_independence]
