@@ -135,7 +135,9 @@ def mcc1d_bwd(gradY, x, weight, mask_or_null, gradX, gradWeight, workspace, stre
 
 
 def tensors(gradY, x, weight, mask, gradX, gradWeight) -> Mcc1dTensors:
-    """Descriptor of torch tensors (their data pointers and element strides)."""
+    """Descriptor of torch tensors (their data pointers and element strides).
+    It holds raw pointers only: keep the tensors (and any view's base) alive
+    until the work enqueued with it has completed."""
     t = Mcc1dTensors()
     t.gradY, t.x, t.weight = gradY.data_ptr(), x.data_ptr(), weight.data_ptr()
     t.gradY_strides[:] = list(gradY.stride())
@@ -149,7 +151,9 @@ def tensors(gradY, x, weight, mask, gradX, gradWeight) -> Mcc1dTensors:
 
 
 def fwd_tensors(x, weight, mask, y) -> Mcc1dFwdTensors:
-    """Forward descriptor of torch tensors (data pointers and element strides)."""
+    """Forward descriptor of torch tensors (data pointers and element strides).
+    It holds raw pointers only: keep the tensors (and any view's base) alive
+    until the work enqueued with it has completed."""
     t = Mcc1dFwdTensors()
     t.x, t.weight, t.y = x.data_ptr(), weight.data_ptr(), y.data_ptr()
     t.x_strides[:] = list(x.stride())
@@ -241,6 +245,8 @@ def forward(x, weight, mask=None, *, y=None, stream=None):
         t = fwd_tensors(x, weight, mask, y)
         nb = mcc1d_fwd_ex_workspace_size(t, S, B, H, W, x.dtype)
         ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=x.device)
+        if isinstance(stream, torch.cuda.Stream):
+            ws.record_stream(stream)   # not reused before the call has run on `stream`
         mcc1d_fwd_ex(t, S, B, H, W, x.dtype, ws, nb, stream)
     return y
 
@@ -341,6 +347,8 @@ def backward(gradY, x, weight, mask=None, *, gradX=None, gradWeight=None, worksp
         nbytes = mcc1d_bwd_ex_workspace_size(desc, S, B, H, W, code)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=gradY.device)
+        if isinstance(stream, torch.cuda.Stream):
+            workspace.record_stream(stream)   # not reused before the call has run on `stream`
     wsb = workspace.numel() * workspace.element_size()
     if dense:
         mcc1d_bwd(gradY, x, weight, mask, gradX, gradWeight, workspace, stream, S, B, H, W, code, wsb)

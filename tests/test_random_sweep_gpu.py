@@ -127,3 +127,46 @@ def test_random_case(n):
     assert ulp <= GX_MAX_ULP, f"gradX off by {ulp} ulp"
     ratio = gradw_ratio(gwb, ref["gw_exact"], ref["gw_abs"], dt)
     assert ratio <= 1.0, f"gradWeight error is {ratio:.3f} x tolerance"
+
+
+N_FWD_CASES = 80
+
+
+def draw_fwd_case(n):
+    c = draw_case(20000 + n)
+    c["W"] = int(np.random.default_rng(30000 + n).integers(1, 9))
+    return c
+
+
+FWD_CASES = [draw_fwd_case(n) for n in range(N_FWD_CASES)]
+
+
+@pytest.mark.parametrize("n", range(N_FWD_CASES), ids=[f"{n}-{case_id(c)}" for n, c in enumerate(FWD_CASES)])
+def test_random_forward_case(n):
+    """The forward on the same kind of draws: the strided call (any layout of
+    x, [H,W]-memory weight, [S,B]-memory mask) gives the same bits as the
+    dense call, within 1 ulp of the oracle."""
+    c = FWD_CASES[n]
+    S, B, H, W, dt = c["S"], c["B"], c["H"], c["W"], c["dt"]
+    wl = datagen.Workload("fsweep", S, B, H, dt, W=W, mask=c["mask"])
+    inp = datagen.generate(wl, seed=n)
+    x, w = to_device(inp["x"], dt), to_device(inp["w"], dt)
+    mask = None if inp["mask"] is None else torch.from_numpy(inp["mask"]).cuda()
+    stream = torch.cuda.current_stream()
+    y = torch.full((S, B, H), float("nan"), dtype=x.dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.mcc1d_fwd(x, w, mask, y, stream, S, B, H, W, dt, status)
+    wv = w.t().contiguous().t() if c["w_t"] else w
+    mv = mask.t().contiguous().t() if (c["m_t"] and mask is not None) else mask
+    y2 = torch.full((S, B, H), float("nan"), dtype=x.dtype, device="cuda")
+    xv = view3(x, c["layout"])          # held: the descriptor keeps only raw pointers
+    t = m.fwd_tensors(xv, wv, mv, y2)
+    nb = m.mcc1d_fwd_ex_workspace_size(t, S, B, H, W, dt)
+    ws = torch.full((max(nb, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+    m.mcc1d_fwd_ex(t, S, B, H, W, dt, ws, nb, stream, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    yb = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(yb, y2.view(torch.int16).cpu().numpy().view(np.uint16))
+    ref = oracle.fwd_bits(S, B, H, W, dt, inp["x"], inp["w"], inp["mask"])
+    assert max_ulp(yb, ref) <= GX_MAX_ULP
