@@ -12,6 +12,7 @@ when the oracle disagrees with what the operator page (CANN
 * the adjoint identity <y, gradY> = <x, gradX> = <w, gradWeight>;
 * PyTorch's CPU autograd of a float64 depthwise ``conv1d`` (a library routine
   that shares nothing with the oracle);
+* sum|terms| of gradWeight (its tolerance scale) summed in numpy;
 * numpy's / torch's 16-bit conversions for the oracle's own rounding.
 
 The same functions run against deliberately broken copies of the oracle in
@@ -357,6 +358,44 @@ def pin_forward_rounding(orc):
         assert np.all(dec(yb, dt)[(mask.T == 0)] == 0)
 
 
+def pin_gradw_abs(orc):
+    """sum|terms| of gradWeight(k,h), the scale its tolerance is stated
+    against, is the sum over j and i of |gYm(i+W-1-k,j,h) * x(i,j,h)| with
+    every term of the formula counted once: the shift of the pair, the mask
+    and the zero padding past S all as in gradWeight itself. Computed here
+    in numpy from independently decoded small dyadic values (every product
+    and sum exact), for W = 1..8, with masks and with S shorter than W."""
+    rng = np.random.default_rng(47)
+    for dt in ("bf16", "fp16"):
+        for W in range(1, 9):
+            for S in (1, 2, 5, 9):
+                for B in (1, 2):
+                    H = 3
+                    gy = small_dyadic_bits(rng, (S, B, H), dt)
+                    x = small_dyadic_bits(rng, (S, B, H), dt)
+                    w = small_dyadic_bits(rng, (W, H), dt)
+                    mask = (rng.random((B, S)) < 0.6).astype(np.uint8) if B == 2 else None
+                    r = orc.bwd(S, B, H, W, dt, gy, x, w, mask, want_gx=False)
+                    gym = masked_gy(dec(gy, dt), mask, S, B)
+                    xv = dec(x, dt)
+                    ex = np.zeros((W, H))
+                    for k in range(W):
+                        shift = W - 1 - k
+                        if shift < S:
+                            ex[k] = np.abs(gym[shift:] * xv[: S - shift]).sum(axis=(0, 1))
+                    assert np.array_equal(r["gw_abs"], ex), (dt, W, S, B)
+    # a case with a closed form: all-ones inputs, no mask, every term +1, so
+    # sum|terms| equals gradWeight's pair counts B*(S-(W-1-k)), clamped at 0
+    for W in (1, 3, 8):
+        S, B, H = 6, 2, 2
+        one = enc(1.0, "bf16")
+        ones = np.full((S, B, H), one, np.uint16)
+        r = orc.bwd(S, B, H, W, "bf16", ones, ones, np.full((W, H), one, np.uint16), None,
+                    want_gx=False)
+        ex = np.array([B * max(S - (W - 1 - k), 0) for k in range(W)], np.float64)
+        assert np.array_equal(r["gw_abs"], np.broadcast_to(ex[:, None], (W, H))), W
+
+
 # ---------------------------------------------------------------- conversions
 def pin_converters(orc):
     """Decoding every 16-bit pattern, and rounding doubles to 16 bits (ties to
@@ -430,5 +469,5 @@ def pin_thread_independence(orc):
 
 ALL_PINS = [pin_golden, pin_closed_form_ones, pin_shift_identities, pin_mask_special_cases,
             pin_s1, pin_batch_independence, pin_jacobian_bruteforce, pin_adjoint_identity,
-            pin_torch_autograd, pin_forward_torch, pin_forward_rounding, pin_converters, pin_gradx_at,
-            pin_thread_independence]
+            pin_torch_autograd, pin_gradw_abs, pin_forward_torch, pin_forward_rounding, pin_converters,
+            pin_gradx_at, pin_thread_independence]

@@ -44,6 +44,18 @@ MUTANTS = {
                                     "acc += g * mcc1d_oracle_to_double(w[k * H + h], dtype);"),
     # implied forward with the taps reversed (the transposition pins must see it)
     "forward_taps_reversed": ("int64_t s = t - (W - 1) + k;", "int64_t s = t - k;"),
+    # sum|terms| of gradWeight summed with signs (no absolute value)
+    "gradw_abs_signed": ("mag[k * H + h] += fabs(t);", "mag[k * H + h] += t;"),
+    # sum|terms| taken over the unshifted pair gYm(i) * x(i) for every tap
+    "gradw_abs_unshifted": ("mag[k * H + h] += fabs(t);",
+                            "mag[k * H + h] += fabs(gym(tab, gy, mask, S, B, H, i, j, h) * "
+                            "tab[x[(i * B + j) * H + h]]);"),
+    # sum|terms| of the unmasked gradY (the mask left out of the scale only)
+    "gradw_abs_unmasked": ("mag[k * H + h] += fabs(t);",
+                           "mag[k * H + h] += fabs(gym(tab, gy, NULL, S, B, H, i + W - 1 - k, j, h) * "
+                           "tab[x[(i * B + j) * H + h]]);"),
+    # sum|terms| twice too large
+    "gradw_abs_doubled": ("mag[k * H + h] += fabs(t);", "mag[k * H + h] += 2.0 * fabs(t);"),
 }
 
 
