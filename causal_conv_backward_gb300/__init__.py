@@ -17,4 +17,5 @@ from ._lib import (  # noqa: F401
     mcc1d_version, Mcc1dTensors, tensors, mcc1d_bwd_ex, mcc1d_bwd_ex_workspace_size,
     mcc1d_fwd, forward, mcc1d_bwd_host, mcc1d_plan_describe, PLAN_BWD, PLAN_BWD_EX, PLAN_FWD,
     mcc1d_selftest_wait, Mcc1dFwdTensors, fwd_tensors, mcc1d_fwd_ex, mcc1d_fwd_ex_workspace_size,
+    PLAN_SMS, mcc1d_check_sm_count, mcc1d_device_sm_count,
 )

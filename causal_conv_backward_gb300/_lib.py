@@ -16,7 +16,9 @@ STATUS = {
     561003: "MCC1D_ERR_WORKSPACE",
     561100: "MCC1D_ERR_CUDA",
     561101: "MCC1D_ERR_DEVICE_TIMEOUT",
+    561102: "MCC1D_ERR_DEVICE",
 }
+PLAN_SMS = 152
 
 _lock = threading.Lock()
 _lib = None
@@ -91,6 +93,10 @@ def load():
         lib.mcc1d_fwd_ex_workspace_size.restype = i32
         lib.mcc1d_fwd_ex.argtypes = [ctypes.POINTER(Mcc1dFwdTensors), i64, i64, i64, i64, i32, vp, u64, vp, vp]
         lib.mcc1d_fwd_ex.restype = i32
+        lib.mcc1d_check_sm_count.argtypes = [i32]
+        lib.mcc1d_check_sm_count.restype = i32
+        lib.mcc1d_device_sm_count.argtypes = [ctypes.POINTER(i32)]
+        lib.mcc1d_device_sm_count.restype = i32
         lib.mcc1d_selftest_wait.argtypes = [vp, i32, vp]
         lib.mcc1d_selftest_wait.restype = i32
         _lib = lib
@@ -274,6 +280,21 @@ def mcc1d_bwd_device_status(workspace, stream=None) -> int:
     st = load().mcc1d_bwd_device_status(_ptr(workspace), stream or None, ctypes.byref(out))
     if st != 0:
         raise Mcc1dError(st, "mcc1d_bwd_device_status")
+    return int(out.value)
+
+
+def mcc1d_check_sm_count(sm_count: int) -> int:
+    """The status every launching call returns for a device with this many
+    SMs (MCC1D_OK, or MCC1D_ERR_DEVICE below the plans' 152)."""
+    return int(load().mcc1d_check_sm_count(int(sm_count)))
+
+
+def mcc1d_device_sm_count() -> int:
+    """SM count of the current device, as the library reads it."""
+    out = ctypes.c_int32(0)
+    st = load().mcc1d_device_sm_count(ctypes.byref(out))
+    if st != 0:
+        raise Mcc1dError(st, "mcc1d_device_sm_count")
     return int(out.value)
 
 

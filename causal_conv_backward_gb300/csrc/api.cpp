@@ -8,6 +8,7 @@
 
 #include <string>
 
+#include "device.h"
 #include "launch.h"
 #include "mcc1d.h"
 #include "plan.h"
@@ -50,6 +51,9 @@ extern "C" int32_t mcc1d_bwd(const void *gradY, const void *x, const void *weigh
         return kErrInvalid;
     if (workspace_bytes < p.ws_bytes)
         return kErrWorkspace;
+    const int32_t dv = check_current_device();
+    if (dv != kOk)
+        return dv;
     return launch_bwd(p, dense_layout(S, B, H), gradY, x, weight, mask_or_null, gradX, gradWeight,
                       workspace, static_cast<cudaStream_t>(stream));
 }
@@ -91,6 +95,9 @@ extern "C" int32_t mcc1d_bwd_host(const void *gradY, const void *x, const void *
         return kErrInvalid;
     if (workspace_bytes < p.ws_bytes)
         return kErrWorkspace;
+    const int32_t dv = check_current_device();
+    if (dv != kOk)
+        return dv;
     const void *gy_d = device_address(gradY), *x_d = device_address(x), *w_d = device_address(weight);
     void *gx_d = device_address(gradX), *gw_d = device_address(gradWeight);
     const void *m_d = mask_or_null ? device_address(mask_or_null) : nullptr;
@@ -200,6 +207,9 @@ extern "C" int32_t mcc1d_bwd_ex(const mcc1d_tensors *t, int64_t S, int64_t B, in
         return kErrInvalid;
     if (workspace_bytes < e.bytes)
         return kErrWorkspace;
+    const int32_t dv = check_current_device();
+    if (dv != kOk)
+        return dv;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const void *gy = t->gradY, *x = t->x;
@@ -253,6 +263,9 @@ extern "C" int32_t mcc1d_fwd(const void *x, const void *weight, const uint8_t *m
         return st;
     if (!aligned16(x) || !aligned16(weight) || !aligned16(y))
         return kErrInvalid;
+    st = check_current_device();
+    if (st != kOk)
+        return st;
     Plan p;
     st = fwd_plan(S, B, H, W, dtype, &p);
     if (st != kOk)
@@ -341,6 +354,9 @@ extern "C" int32_t mcc1d_fwd_ex(const mcc1d_fwd_tensors *t, int64_t S, int64_t B
         if (workspace_bytes < e.bytes)
             return kErrWorkspace;
     }
+    st = check_current_device();
+    if (st != kOk)
+        return st;
     Plan p;
     st = fwd_plan(S, B, H, W, dtype, &p);
     if (st != kOk)
@@ -468,6 +484,19 @@ extern "C" int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, 
     return kOk;
 }
 
+extern "C" int32_t mcc1d_check_sm_count(int32_t sm_count) { return check_sm_count(sm_count); }
+
+extern "C" int32_t mcc1d_device_sm_count(int32_t *sm_count_out)
+{
+    if (!sm_count_out)
+        return kErrNull;
+    const int32_t n = current_device_sm_count();
+    if (n <= 0)
+        return kErrCuda;
+    *sm_count_out = n;
+    return kOk;
+}
+
 extern "C" const char *mcc1d_status_string(int32_t status)
 {
     switch (status) {
@@ -478,6 +507,7 @@ extern "C" const char *mcc1d_status_string(int32_t status)
     case kErrWorkspace: return "MCC1D_ERR_WORKSPACE: workspace smaller than mcc1d_bwd_workspace_size reported";
     case kErrCuda: return "MCC1D_ERR_CUDA: a CUDA runtime call failed";
     case kErrTimeout: return "MCC1D_ERR_DEVICE_TIMEOUT: a device-side wait gave up; outputs are not valid";
+    case kErrDevice: return "MCC1D_ERR_DEVICE: the current device has fewer SMs than the launch plans assume (152)";
     default: return "unknown mcc1d status";
     }
 }

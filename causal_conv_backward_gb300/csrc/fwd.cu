@@ -23,6 +23,7 @@
 #include <atomic>
 
 #include "device_common.cuh"
+#include "device.h"
 #include "launch.h"
 #include "plan.h"
 
@@ -438,18 +439,20 @@ int32_t launch_fwd(const Plan &pl, const Layout &L, const void *x, const void *w
     FwdFn fn = fwd_kernel(pl.dtype, pl.vec, pl.W);
     if (fn == nullptr)
         return kErrCuda;
-    static std::atomic<uint64_t> done[4 * (kMaxW + 1)];
+    // the shared-memory attribute, once per (instance, device, context): a
+    // context created after a device reset starts without it
+    static std::atomic<unsigned long long> done[4 * (kMaxW + 1)][64];
     const int slot_id = (pl.dtype * 2 + (pl.vec == 4 ? 1 : 0)) * (kMaxW + 1) + pl.W;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return kErrCuda;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(done[slot_id].load(std::memory_order_acquire) & bit)) {
+    const unsigned long long ctx = current_context_id();
+    if (ctx == 0 || done[slot_id][dev].load(std::memory_order_acquire) != ctx) {
         if (cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemDynMax) != cudaSuccess)
             return kErrCuda;
-        done[slot_id].fetch_or(bit, std::memory_order_acq_rel);
+        done[slot_id][dev].store(ctx != 0 ? ctx : current_context_id(), std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.ncta);

@@ -43,6 +43,7 @@
 #include <mutex>
 
 #include "bwd_main.cuh"
+#include "device.h"
 #include "device_common.cuh"
 #include "launch.h"
 #include "plan.h"
@@ -175,19 +176,21 @@ static MainFn main_kernel(int dtype, int R, int vec, int W)
     return vec == 4 ? main_for<1, 2>(R) : main_for<1, 4>(R);
 }
 
-// cudaFuncSetAttribute once per (kernel, device).
+// cudaFuncSetAttribute once per (kernel, device, context): a context created
+// after a device reset starts without the attribute.
 static bool ensure_smem_attr(const void *fn)
 {
+    constexpr int kSlots = 128, kDevs = 64;
     static std::mutex mu;
-    static const void *fns[128];
-    static uint64_t devmask[128];
+    static const void *fns[kSlots];
+    static unsigned long long ctx_of[kSlots][kDevs];   // context the attribute was set in
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs)
         return false;
-    const uint64_t bit = 1ull << (dev & 63);
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
     int slot = -1;
-    for (int i = 0; i < 128; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
         if (fns[i] == fn) {
             slot = i;
             break;
@@ -200,13 +203,14 @@ static bool ensure_smem_attr(const void *fn)
     }
     if (slot < 0)
         return false;
-    if (devmask[slot] & bit)
+    if (ctx != 0 && ctx_of[slot][dev] == ctx)
         return true;
     // leave room for the kernel's few bytes of static shared memory
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemDynMax) != cudaSuccess)
         return false;
-    devmask[slot] |= bit;
+    // the call above makes the device's primary context current if none was
+    ctx_of[slot][dev] = ctx != 0 ? ctx : current_context_id();
     return true;
 }
 
@@ -251,8 +255,12 @@ int32_t launch_reduce(const Plan &pl, void *workspace, void *gradWeight, cudaStr
 int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_t S, int64_t B,
                     int64_t H, cudaStream_t stream)
 {
+    // grid-stride gather: eight 256-thread CTAs per SM of the device
+    int sms = current_device_sm_count();
+    if (sms <= 0)
+        sms = kNumSMs;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(kNumSMs * 8));
+    cfg.gridDim = dim3((unsigned)(sms * 8));
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
     if (cudaLaunchKernelEx(&cfg, mcc1d_pack, static_cast<const uint16_t *>(src), strides[0], strides[1],

@@ -12,6 +12,7 @@
 
 #include <mutex>
 
+#include "device.h"
 #include "launch.h"
 #include "mcc1d.h"
 #include "plan.h"
@@ -26,23 +27,38 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[MCC1D_NOALLOC_SCRATCH
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices];
+
+// The array's device address, cached per device together with the unique id
+// of the context it was looked up in. A device reset (cudaDeviceReset, or a
+// host framework that releases and re-creates the primary context) loads the
+// library's module again in a new context, where the array may sit at a new
+// address; the changed context id makes the next call look it up again.
+struct ScratchSlot {
+    unsigned long long ctx_id;   // 0: unknown
+    void *addr;
+};
+ScratchSlot g_scratch[kMaxDevices];
 
 // Device address of g_noalloc_scratch on the current device. The first call
-// on a device looks it up with that device current; later calls reuse it.
+// on a device (and the first after its context was re-created) looks it up
+// with that device current; later calls reuse it.
 int32_t scratch_address(void **out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return kErrCuda;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchSlot &slot = g_scratch[dev];
+    if (slot.addr == nullptr || ctx == 0 || slot.ctx_id != ctx) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
             return kErrCuda;
-        g_scratch_addr[dev] = ptr;
+        slot.addr = ptr;
+        // the lookup makes the device's primary context current if none was
+        slot.ctx_id = ctx != 0 ? ctx : current_context_id();
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return kOk;
 }
 
@@ -66,6 +82,9 @@ extern "C" int32_t mcc1d_bwd_noalloc(const void *gradY, const void *x, const voi
     // The shape's scratch must fit the fixed array.
     if (p.ws_bytes > (uint64_t)MCC1D_NOALLOC_SCRATCH_BYTES)
         return kErrWorkspace;
+    const int32_t dv = check_current_device();
+    if (dv != kOk)
+        return dv;
     void *scratch = nullptr;
     const int32_t sa = scratch_address(&scratch);
     if (sa != kOk)

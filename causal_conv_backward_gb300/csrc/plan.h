@@ -24,7 +24,7 @@ constexpr int kTwoCtaMaxW = 5;        // widths 4 .. kTwoCtaMaxW run two CTAs pe
 constexpr int kRegsOneCta = 168;      // register bound of the main kernel (288 threads, one CTA)
 constexpr int kRegsTwoCta = 96;       // ... and of its two-CTA form (mcc1d_bwd_main_x2)
 constexpr int kDeepMinRowsPerCta = 256;  // CTA range long enough for 14-row stages
-constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs
+constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs (MCC1D_PLAN_SMS; checked per device)
 constexpr int kSmemPerSM = 233472;    // 228 KB of shared memory per SM
 constexpr int kSmemPerCtaMax = 232448;// 227 KB opt-in maximum per CTA
 constexpr int kSmemReservedPerCta = 1024;
@@ -52,6 +52,7 @@ enum : int32_t {
     kErrWorkspace = 561003,
     kErrCuda = 561100,
     kErrTimeout = 561101,
+    kErrDevice = 561102,
 };
 
 struct Plan {

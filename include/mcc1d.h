@@ -78,8 +78,17 @@ typedef enum {
     MCC1D_ERR_CUDA = 561100,
     /* Reported by mcc1d_bwd_device_status: a device-side wait of the last
      * call gave up after its time limit and the outputs are not valid. */
-    MCC1D_ERR_DEVICE_TIMEOUT = 561101
+    MCC1D_ERR_DEVICE_TIMEOUT = 561101,
+    /* The current device has fewer SMs than the launch plans are cut for
+     * (MCC1D_PLAN_SMS): part of every grid would run as a second wave at
+     * about twice the time. Returned by every call that launches, before
+     * anything is enqueued. */
+    MCC1D_ERR_DEVICE = 561102
 } mcc1d_status;
+
+/* SMs the launch plans assume (GB300: two dies of 76). The plans are a
+ * function of the shape alone, so results never depend on the device. */
+#define MCC1D_PLAN_SMS 152
 
 /*
  * Phase 1 (page: aclnnMaskedCausalConv1dBackwardGetWorkspaceSize).
@@ -120,8 +129,9 @@ int32_t mcc1d_bwd_workspace_size(int64_t S, int64_t B, int64_t H, int64_t W, int
  * MCC1D_ERR_PARAM_NULLPTR (a null tensor or workspace pointer),
  * MCC1D_ERR_PARAM_INVALID (dtype, or a pointer not 16-byte aligned),
  * MCC1D_ERR_INNER_TILING_ERROR (shape), MCC1D_ERR_WORKSPACE (workspace_bytes
- * too small), MCC1D_ERR_CUDA (a launch failed; the CUDA error is left for
- * cudaGetLastError to report).
+ * too small), MCC1D_ERR_DEVICE (the current device has fewer than
+ * MCC1D_PLAN_SMS SMs), MCC1D_ERR_CUDA (a launch failed; the CUDA error is
+ * left for cudaGetLastError to report).
  */
 int32_t mcc1d_bwd(const void *gradY, const void *x, const void *weight,
                   const uint8_t *mask_or_null, void *gradX, void *gradWeight,
@@ -242,8 +252,15 @@ int32_t mcc1d_bwd_device_status(const void *workspace, void *stream, int32_t *st
  *    scratch word before they read it, so nothing needs clearing between calls.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture begins.
- *  - mcc1d_bwd_device_status does not apply to this call.
+ *    before any stream capture begins. The address is cached with the id of
+ *    the context it was found in: after a device reset (cudaDeviceReset, or
+ *    a framework re-creating the primary context) the next call looks it up
+ *    again, since the new context may place the array elsewhere.
+ *  - A device-side wait that gives up (the bounded waits described under
+ *    mcc1d_bwd_device_status) goes unreported on this call: the status words
+ *    live in the shared array, which no caller can read, so the call returns
+ *    MCC1D_OK with gradX and gradWeight incomplete. Callers that need to
+ *    detect that use mcc1d_bwd and mcc1d_bwd_device_status.
  * Errors: as mcc1d_bwd, plus MCC1D_ERR_WORKSPACE for a shape too large for the
  * array and MCC1D_ERR_CUDA if the address lookup fails.
  */
@@ -334,6 +351,18 @@ int32_t mcc1d_fwd_ex(const mcc1d_fwd_tensors *t, int64_t S, int64_t B, int64_t H
 enum { MCC1D_PLAN_BWD = 0, MCC1D_PLAN_BWD_EX = 1, MCC1D_PLAN_FWD = 2 };
 int32_t mcc1d_plan_describe(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
                             int32_t kind, char *buf, uint64_t buf_bytes, uint64_t *needed_out);
+
+/*
+ * Device check (no counterpart on the page). Every call that launches
+ * compares the current device's SM count (cudaDevAttrMultiProcessorCount,
+ * read once per device) with MCC1D_PLAN_SMS and refuses a smaller device with
+ * MCC1D_ERR_DEVICE. mcc1d_check_sm_count applies that rule to a given count
+ * (host only; MCC1D_OK or MCC1D_ERR_DEVICE). mcc1d_device_sm_count writes
+ * the current device's count to *sm_count_out (MCC1D_ERR_PARAM_NULLPTR for a
+ * null pointer, MCC1D_ERR_CUDA when the runtime cannot say).
+ */
+int32_t mcc1d_check_sm_count(int32_t sm_count);
+int32_t mcc1d_device_sm_count(int32_t *sm_count_out);
 
 /*
  * Self-test of the bounded device-side wait (no counterpart on the page).

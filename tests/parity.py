@@ -59,6 +59,66 @@ def gradw_ratio(gpu_bits, exact, abs_sum, dtype) -> float:
     return float(np.max(np.abs(g - exact) / tol))
 
 
+# ------------------------------------------------------------------ guard bands
+# Every output and workspace a parity test hands to the library is carved out
+# of a larger allocation with GUARD_BYTES of a fixed pattern before and after
+# it. After the call, check_guards() asserts that the pattern is intact, so a
+# store past either end of a buffer (which would otherwise land silently in
+# the caching allocator's memory) fails the test.
+GUARD_BYTES = 4096
+GUARD_PATTERN = 0xC3
+
+
+class _Guard:
+    __slots__ = ("base", "nbytes")
+
+    def __init__(self, base, nbytes):
+        self.base = base
+        self.nbytes = nbytes
+
+
+def guarded_empty(shape, dtype, device="cuda", *, pin_memory=False):
+    """An uninitialised tensor of `shape`/`dtype` (contiguous, 256-byte
+    aligned) with guard regions around it; check it with check_guards()."""
+    import torch
+    shape = tuple(int(d) for d in shape)
+    elem = torch.empty((), dtype=dtype).element_size()
+    nbytes = int(np.prod(shape, dtype=np.int64)) * elem
+    inner = (nbytes + 255) // 256 * 256
+    if pin_memory:
+        base = torch.empty(2 * GUARD_BYTES + inner, dtype=torch.uint8, pin_memory=True)
+    else:
+        base = torch.empty(2 * GUARD_BYTES + inner, dtype=torch.uint8, device=device)
+    base.fill_(GUARD_PATTERN)
+    t = base[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype).view(shape)
+    t._mcc1d_guard = _Guard(base, nbytes)
+    return t
+
+
+def guarded_full(shape, dtype, fill_byte, device="cuda", *, pin_memory=False):
+    """guarded_empty() with every byte of the tensor set to `fill_byte`."""
+    import torch
+    t = guarded_empty(shape, dtype, device, pin_memory=pin_memory)
+    if t.numel():
+        t.view(-1).view(torch.uint8).fill_(fill_byte)
+    return t
+
+
+def check_guards(*tensors, what=""):
+    """Assert that the guard regions of every tensor made by guarded_empty()
+    still hold the pattern (call after the work on them has completed)."""
+    for k, t in enumerate(tensors):
+        g = getattr(t, "_mcc1d_guard", None) if t is not None else None
+        if g is None:
+            continue
+        head = g.base[:GUARD_BYTES]
+        tail = g.base[GUARD_BYTES + g.nbytes:]
+        bad_head = int((head != GUARD_PATTERN).sum())
+        bad_tail = int((tail != GUARD_PATTERN).sum())
+        assert bad_head == 0 and bad_tail == 0, (
+            f"{what} buffer {k}: {bad_head} guard bytes before and {bad_tail} after it were overwritten")
+
+
 def to_device(bits: np.ndarray, dtype: str, device="cuda"):
     import torch
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
@@ -72,7 +132,8 @@ def run_cuda(inp: dict, S, B, H, dtype, *, W=3, stream=None, workspace=None, fil
              mask_override=_KEEP):
     """Run the CUDA path once through the C ABI; returns (gx_bits, gw_bits,
     device_status, workspace). Outputs are pre-filled with NaN patterns so an
-    unwritten element cannot pass."""
+    unwritten element cannot pass; outputs and workspace sit between guard
+    regions that are checked after the call."""
     import torch
     import causal_conv_backward_gb300 as m
 
@@ -81,22 +142,22 @@ def run_cuda(inp: dict, S, B, H, dtype, *, W=3, stream=None, workspace=None, fil
     w = to_device(inp["w"], dtype)
     mask = inp["mask"] if mask_override is _KEEP else mask_override
     md = None if mask is None else torch.from_numpy(np.ascontiguousarray(mask)).cuda()
-    gx = torch.empty_like(gy)
-    gw = torch.empty_like(w)
+    gx = guarded_empty(gy.shape, gy.dtype)
+    gw = guarded_empty(w.shape, w.dtype)
     if fill_outputs:
         gx.view(torch.int16).fill_(-1)   # 0xFFFF: a NaN in both formats
         gw.view(torch.int16).fill_(-1)
     code = m.dtype_code(dtype)
     nbytes = m.mcc1d_bwd_workspace_size(S, B, H, W, code, md is not None)
     if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-        workspace.fill_(0xFF)
+        workspace = guarded_full((nbytes,), torch.uint8, 0xFF)
     if stream is None:
         stream = torch.cuda.current_stream()
     else:
         stream.wait_stream(torch.cuda.current_stream())  # inputs were made on torch's stream
     m.mcc1d_bwd(gy, x, w, md, gx, gw, workspace, stream, S, B, H, W, code, workspace.numel())
     status = m.mcc1d_bwd_device_status(workspace, stream)  # synchronises `stream`
+    check_guards(gx, gw, workspace, what="mcc1d_bwd gradX/gradWeight/workspace")
     gxb = gx.view(torch.int16).cpu().numpy().view(np.uint16)
     gwb = gw.view(torch.int16).cpu().numpy().view(np.uint16)
     return gxb, gwb, status, workspace

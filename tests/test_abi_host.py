@@ -101,11 +101,25 @@ def test_bwd_workspace_too_small(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, NULLPTR, INVALID, SHAPE, WORKSPACE, 561100, 561101):
+    for code in (0, NULLPTR, INVALID, SHAPE, WORKSPACE, 561100, 561101, 561102):
         s = m.mcc1d_status_string(code)
         assert s.startswith("MCC1D_")
     assert m.mcc1d_status_string(42) == "unknown mcc1d status"
     assert m.mcc1d_version() >= 100
+
+
+def test_sm_count_check_refuses_a_smaller_device(lib):
+    """The plans cut every shape into 152 x (CTAs per SM) persistent CTAs; a
+    device with fewer SMs would run part of each grid as a second wave, so
+    every launching call refuses it with MCC1D_ERR_DEVICE. The rule, applied
+    to fake counts (no device needed):"""
+    assert m.PLAN_SMS == 152
+    for n in (1, 76, 148, 151):
+        assert m.mcc1d_check_sm_count(n) == 561102, n
+        assert "fewer SMs" in m.mcc1d_status_string(m.mcc1d_check_sm_count(n))
+    for n in (152, 160, 264):
+        assert m.mcc1d_check_sm_count(n) == 0, n
+    assert lib.mcc1d_device_sm_count(None) == NULLPTR
 
 
 # ------------------------------------------------------------- strided calls

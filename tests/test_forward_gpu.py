@@ -11,7 +11,7 @@ import pytest
 
 import datagen
 import oracle
-from parity import GX_MAX_ULP, max_ulp, to_device, values
+from parity import GX_MAX_ULP, check_guards, guarded_full, max_ulp, to_device, values
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -32,12 +32,12 @@ def run_fwd(inp, S, B, H, dt, mask_override=None, use_override=False, W=3):
     w = to_device(inp["w"], dt)
     mask = mask_override if use_override else inp["mask"]
     md = None if mask is None else torch.from_numpy(np.ascontiguousarray(mask)).cuda()
-    y = torch.empty_like(x)
-    y.view(torch.int16).fill_(-1)
+    y = guarded_full(x.shape, x.dtype, 0xFF)   # NaN patterns
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     m.mcc1d_fwd(x, w, md, y, torch.cuda.current_stream(), S, B, H, W, dt, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    check_guards(y, what="mcc1d_fwd y")
     return y.view(torch.int16).cpu().numpy().view(np.uint16)
 
 

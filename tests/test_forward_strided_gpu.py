@@ -7,7 +7,7 @@ import pytest
 
 import datagen
 import oracle
-from parity import GX_MAX_ULP, max_ulp, to_device
+from parity import GX_MAX_ULP, check_guards, guarded_full, max_ulp, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -43,20 +43,21 @@ def test_strided_forward_matches_dense(S, B, H, dt, W, layout):
     x, w = to_device(inp["x"], dt), to_device(inp["w"], dt)
     mask = torch.from_numpy(inp["mask"]).cuda()
     stream = torch.cuda.current_stream()
-    y_dense = torch.empty_like(x)
+    y_dense = guarded_full(x.shape, x.dtype, 0xFF)
     m.mcc1d_fwd(x, w, mask, y_dense, stream, S, B, H, W, dt)
     # strided x, [H,W]-memory weight, [S,B]-memory mask
     xv = make_view(x, layout)
     wv = w.t().contiguous().t()
     mv = mask.t().contiguous().t()
-    y = torch.full((S, B, H), float("nan"), dtype=x.dtype, device="cuda")
+    y = guarded_full((S, B, H), x.dtype, 0xFF)
     t = m.fwd_tensors(xv, wv, mv, y)
     nb = m.mcc1d_fwd_ex_workspace_size(t, S, B, H, W, dt)
-    ws = torch.full((max(nb, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+    ws = guarded_full((max(nb, 16),), torch.uint8, 0xFF)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     m.mcc1d_fwd_ex(t, S, B, H, W, dt, ws, nb, stream, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    check_guards(y_dense, y, ws, what="mcc1d_fwd / mcc1d_fwd_ex")
     assert np.array_equal(bits(y), bits(y_dense))
     ref = oracle.fwd_bits(S, B, H, W, dt, inp["x"], inp["w"], inp["mask"])
     assert max_ulp(bits(y), ref) <= GX_MAX_ULP

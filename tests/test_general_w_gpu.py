@@ -10,7 +10,7 @@ import pytest
 
 import datagen
 import oracle
-from parity import GX_MAX_ULP, gradw_ratio, max_ulp, to_device
+from parity import GX_MAX_ULP, check_guards, gradw_ratio, guarded_full, max_ulp, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -29,13 +29,14 @@ def cuda_ready():
 def run_ex(inp, S, B, H, W, dt):
     gy, x, w = (to_device(inp[k], dt) for k in ("gy", "x", "w"))
     mask = None if inp["mask"] is None else torch.from_numpy(inp["mask"]).cuda()
-    gx = torch.full((S, B, H), float("nan"), dtype=gy.dtype, device="cuda")
-    gw = torch.full((W, H), float("nan"), dtype=gy.dtype, device="cuda")
+    gx = guarded_full((S, B, H), gy.dtype, 0xFF)   # NaN patterns
+    gw = guarded_full((W, H), gy.dtype, 0xFF)
     t = m.tensors(gy, x, w, mask, gx, gw)
     nb = m.mcc1d_bwd_ex_workspace_size(t, S, B, H, W, dt)
-    ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws = guarded_full((nb,), torch.uint8, 0xFF)
     m.mcc1d_bwd_ex(t, S, B, H, W, dt, ws, nb, torch.cuda.current_stream())
     assert m.mcc1d_bwd_device_status(ws, torch.cuda.current_stream()) == 0
+    check_guards(gx, gw, ws, what="mcc1d_bwd_ex")
     return gx.view(torch.int16).cpu().numpy().view(np.uint16), gw.view(torch.int16).cpu().numpy().view(np.uint16)
 
 

@@ -10,7 +10,7 @@ import pytest
 
 import datagen
 import oracle
-from parity import GX_MAX_ULP, gradw_ratio, max_ulp, run_cuda
+from parity import GX_MAX_ULP, check_guards, gradw_ratio, guarded_full, max_ulp, run_cuda
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -38,17 +38,15 @@ def run_host(inp, S, B, H, dt, outputs_on_device=False):
     if inp["mask"] is not None:
         mask = torch.empty(inp["mask"].shape, dtype=torch.uint8, pin_memory=True)
         mask.copy_(torch.from_numpy(inp["mask"]))
-    if outputs_on_device:
-        gx = torch.full((S, B, H), -1, dtype=torch.int16, device="cuda")
-        gw = torch.full((3, H), -1, dtype=torch.int16, device="cuda")
-    else:
-        gx = torch.full((S, B, H), -1, dtype=torch.int16, pin_memory=True)
-        gw = torch.full((3, H), -1, dtype=torch.int16, pin_memory=True)
+    pin = not outputs_on_device
+    gx = guarded_full((S, B, H), torch.int16, 0xFF, pin_memory=pin)
+    gw = guarded_full((3, H), torch.int16, 0xFF, pin_memory=pin)
     nb = m.mcc1d_bwd_workspace_size(S, B, H, 3, dt, mask is not None)
-    ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws = guarded_full((nb,), torch.uint8, 0xFF)
     s = torch.cuda.current_stream()
     m.mcc1d_bwd_host(gy, x, w, mask, gx, gw, ws, s, S, B, H, 3, dt, nb)
     assert m.mcc1d_bwd_device_status(ws, s) == 0   # synchronises the stream
+    check_guards(gx, gw, ws, what="mcc1d_bwd_host")
     return gx.cpu().numpy().view(np.uint16), gw.cpu().numpy().view(np.uint16)
 
 

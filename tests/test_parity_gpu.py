@@ -11,7 +11,7 @@ import pytest
 
 import datagen
 import oracle
-from parity import GX_MAX_ULP, gradw_ratio, max_ulp, run_cuda, values
+from parity import GX_MAX_ULP, check_guards, gradw_ratio, guarded_empty, guarded_full, max_ulp, run_cuda, values
 
 torch = pytest.importorskip("torch")
 
@@ -190,12 +190,13 @@ def test_max_size_property():
     gy, x = one, one  # read-only inputs may alias
     w = wv.to(torch.bfloat16).to(dev)
     md = mask.to(dev)
-    gx = torch.empty((S, B, H), dtype=torch.bfloat16, device=dev)
-    gw = torch.empty((3, H), dtype=torch.bfloat16, device=dev)
+    gx = guarded_empty((S, B, H), torch.bfloat16)
+    gw = guarded_empty((3, H), torch.bfloat16)
     nbytes = m.mcc1d_bwd_workspace_size(S, B, H, 3, dt, True)
-    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=dev)
+    ws = guarded_full((nbytes,), torch.uint8, 0xFF)
     m.mcc1d_bwd(gy, x, w, md, gx, gw, ws, torch.cuda.current_stream(), S, B, H, 3, 0, nbytes)
     assert m.mcc1d_bwd_device_status(ws, torch.cuda.current_stream()) == 0
+    check_guards(gx, gw, ws, what="maximum size")
     # gYm(i,j) = mask(j,i); shifted copies with zero padding past S
     mt = md.t().to(torch.float32)                 # [S,B]
     sh = [torch.zeros_like(mt) for _ in range(3)]

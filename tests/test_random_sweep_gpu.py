@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 import datagen
-from parity import GX_MAX_ULP, gradw_ratio, max_ulp, to_device
+from parity import GX_MAX_ULP, check_guards, gradw_ratio, guarded_full, max_ulp, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -99,8 +99,8 @@ def test_random_case(n):
     if c["m_t"]:
         mask = mask.t().contiguous().t()    # [S,B] memory seen as [B,S]
     gy_v, x_v = view3(gy, c["layout"]), view3(x, c["layout"])
-    gx = torch.full((S, B, H), float("nan"), dtype=gy.dtype, device="cuda")
-    gw = torch.full((W, H), float("nan"), dtype=gy.dtype, device="cuda")
+    gx = guarded_full((S, B, H), gy.dtype, 0xFF)   # NaN patterns
+    gw = guarded_full((W, H), gy.dtype, 0xFF)
     stream = torch.cuda.current_stream()
     dense = W == 3 and c["layout"] == "sbh" and not c["w_t"] and not c["m_t"]
 
@@ -108,14 +108,15 @@ def test_random_case(n):
         """One call with the workspace pre-filled with `fill` bytes."""
         if dense:
             nb = m.mcc1d_bwd_workspace_size(S, B, H, W, dt, mask is not None)
-            ws = torch.full((nb,), fill, dtype=torch.uint8, device="cuda")
+            ws = guarded_full((nb,), torch.uint8, fill)
             m.mcc1d_bwd(gy_v, x_v, w, mask, gx, gw, ws, stream, S, B, H, W, dt, nb)
         else:
             t = m.tensors(gy_v, x_v, w, mask, gx, gw)
             nb = m.mcc1d_bwd_ex_workspace_size(t, S, B, H, W, dt)
-            ws = torch.full((nb,), fill, dtype=torch.uint8, device="cuda")
+            ws = guarded_full((nb,), torch.uint8, fill)
             m.mcc1d_bwd_ex(t, S, B, H, W, dt, ws, nb, stream)
         assert m.mcc1d_bwd_device_status(ws, stream) == 0
+        check_guards(gx, gw, ws, what="backward")
         return (gx.view(torch.int16).cpu().numpy().view(np.uint16).copy(),
                 gw.view(torch.int16).cpu().numpy().view(np.uint16).copy())
 
@@ -153,19 +154,20 @@ def test_random_forward_case(n):
     x, w = to_device(inp["x"], dt), to_device(inp["w"], dt)
     mask = None if inp["mask"] is None else torch.from_numpy(inp["mask"]).cuda()
     stream = torch.cuda.current_stream()
-    y = torch.full((S, B, H), float("nan"), dtype=x.dtype, device="cuda")
+    y = guarded_full((S, B, H), x.dtype, 0xFF)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     m.mcc1d_fwd(x, w, mask, y, stream, S, B, H, W, dt, status)
     wv = w.t().contiguous().t() if c["w_t"] else w
     mv = mask.t().contiguous().t() if (c["m_t"] and mask is not None) else mask
-    y2 = torch.full((S, B, H), float("nan"), dtype=x.dtype, device="cuda")
+    y2 = guarded_full((S, B, H), x.dtype, 0xFF)
     xv = view3(x, c["layout"])          # held: the descriptor keeps only raw pointers
     t = m.fwd_tensors(xv, wv, mv, y2)
     nb = m.mcc1d_fwd_ex_workspace_size(t, S, B, H, W, dt)
-    ws = torch.full((max(nb, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+    ws = guarded_full((max(nb, 16),), torch.uint8, 0xFF)
     m.mcc1d_fwd_ex(t, S, B, H, W, dt, ws, nb, stream, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    check_guards(y, y2, ws, what="forward")
     yb = y.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(yb, y2.view(torch.int16).cpu().numpy().view(np.uint16))
     ref = oracle.fwd_bits(S, B, H, W, dt, inp["x"], inp["w"], inp["mask"])

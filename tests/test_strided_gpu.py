@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import datagen
-from parity import GX_MAX_ULP, gradw_ratio, max_ulp, to_device
+from parity import GX_MAX_ULP, check_guards, gradw_ratio, guarded_empty, guarded_full, max_ulp, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -51,21 +51,25 @@ def make_view(dense, layout):
 
 
 def run_dense(gy, x, w, mask, S, B, H, dt):
-    gx = torch.empty_like(gy)
-    gw = torch.empty_like(w)
+    gx = guarded_empty((S, B, H), gy.dtype)
+    gw = guarded_empty((3, H), gy.dtype)
     nb = m.mcc1d_bwd_workspace_size(S, B, H, 3, dt, mask is not None)
-    ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws = guarded_full((nb,), torch.uint8, 0xFF)
     m.mcc1d_bwd(gy, x, w, mask, gx, gw, ws, torch.cuda.current_stream(), S, B, H, 3, dt, nb)
+    torch.cuda.synchronize()
+    check_guards(gx, gw, ws, what="mcc1d_bwd")
     return gx, gw
 
 
 def run_ex(gy, x, w, mask, S, B, H, dt):
-    gx = torch.full((S, B, H), float("nan"), dtype=gy.dtype, device="cuda")
-    gw = torch.full((3, H), float("nan"), dtype=gy.dtype, device="cuda")
+    gx = guarded_full((S, B, H), gy.dtype, 0xFF)   # NaN patterns
+    gw = guarded_full((3, H), gy.dtype, 0xFF)
     t = m.tensors(gy, x, w, mask, gx, gw)
     nb = m.mcc1d_bwd_ex_workspace_size(t, S, B, H, 3, dt)
-    ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws = guarded_full((nb,), torch.uint8, 0xFF)
     m.mcc1d_bwd_ex(t, S, B, H, 3, dt, ws, nb, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    check_guards(gx, gw, ws, what="mcc1d_bwd_ex")
     return gx, gw, nb
 
 
