@@ -14,9 +14,15 @@ token; read weight and write gradWeight), plus tokens*H per second.
 
 --impl reference times the CPU oracle (the plain fp64 C restatement of the
 operation) on the host cores, one bounded sample of the workload per step.
-With N > 1 (launched by torch.distributed.run) every rank runs its own
-replica of the workload (weak scaling, no collective on the data path); the
-timed region is bracketed by barriers and the slowest rank's time is used.
+With N > 1 every rank runs its own replica of the workload on its own GPU
+(weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the slowest rank's time is used. The ranks come
+from torch.distributed.run when it launched the script, else bench.py
+spawns N local processes itself.
+
+After the headline line's timed region, rank 0 of a one-GPU run also times
+the other workloads of the operator's envelope and the forward (outside the
+headline number) and lists them under "workloads".
 """
 from __future__ import annotations
 
@@ -38,6 +44,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fused conv1d-bwd achieved HBM GB/s and % of GB300 peak; tokens*H/sec"
 WORKLOAD = "s16384_b32_h4096_fp16"
 FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 8000.0     # GB300 HBM3e nominal, ~8 TB/s
 CPU_SAMPLE_S = 16384      # cpu_baseline: the whole workload (all positions, batches and H) ...
 CPU_SAMPLE_PASSES = 3     # ... three passes: about 10 s on 16 host cores
 REF_SAMPLE_S = 64         # --impl reference: first 64 positions per step
@@ -70,6 +77,8 @@ def parse_args(argv=None):
                     help="capture the K timed calls in one CUDA graph (removes host launch gaps)")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="run on the first N positions of the workload (small profiling captures)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workloads timed after the headline")
     return ap.parse_args(argv)
 
 
@@ -109,6 +118,36 @@ def barrier(dist, device=None):
             dist.barrier(device_ids=[device.index])
         else:
             dist.barrier()
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _replica_main(rank, world, port, target, args):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), LOCAL_WORLD_SIZE=str(world))
+    target(*args)
+
+
+def spawn_replicas(world: int, target, *args) -> int:
+    """Run target(*args) in `world` new local processes, rank r on GPU r, each
+    with the environment of a one-node torch.distributed job (rendezvous on
+    127.0.0.1). Returns the first nonzero exit code, else 0."""
+    import multiprocessing
+    ctx = multiprocessing.get_context("spawn")   # never fork a process that may hold a CUDA context
+    port = _free_port()
+    procs = [ctx.Process(target=_replica_main, args=(r, world, port, target, args)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    rc = 0
+    for pr in procs:
+        pr.join()
+        rc = rc or (pr.exitcode or 0)
+    return rc
 
 
 # ------------------------------------------------------------------ clocks
@@ -285,12 +324,122 @@ def time_oracle(wl, s_rows: int, steps: int, warmup: int):
 
 
 # ------------------------------------------------------------------ arms
-def gpu_arm(args):
+def device_inputs(wl, dev, pinned_host=False):
+    """The workload's seeded inputs on the device (gy, x, w as 16-bit tensors,
+    mask as bytes or None), plus the host copies they came from."""
     import numpy as np
     import torch
 
-    import causal_conv_backward_gb300 as m
     import datagen
+
+    def pinned(shape, dt):
+        tdt = {np.uint16: torch.int16, np.uint8: torch.uint8}[dt]
+        return torch.empty(shape, dtype=tdt, pin_memory=True)
+
+    host = datagen.generate(wl, seed=0, alloc=pinned if pinned_host else None)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+
+    def dev16(a):
+        t = a if isinstance(a, torch.Tensor) else torch.from_numpy(a.view(np.int16))
+        return t.to(dev).view(tdt)
+
+    d = {"gy": dev16(host["gy"]), "x": dev16(host["x"]), "w": dev16(host["w"]),
+         "mask": None if host["mask"] is None else (
+             host["mask"] if isinstance(host["mask"], torch.Tensor) else torch.from_numpy(host["mask"])).to(dev)}
+    return d, host
+
+
+def time_calls(step, K, stream, flush_buf=None):
+    """K calls of step(), each bracketed by its own CUDA events on `stream`;
+    with flush_buf, the buffer is rewritten before every call (outside the
+    events) so no call finds the previous one's lines in L2. Returns the
+    per-call seconds and the seconds of the whole region."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(K):
+        if flush_buf is not None:
+            flush_buf.fill_(k & 255)
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) / 1e3 for a, b in ev], start.elapsed_time(end) / 1e3
+
+
+# Workloads timed after the headline (one GPU): the operator's other
+# configurations, the headline workload without a mask, and its forward.
+EXTRAS = [
+    ("s64_b2_h384_bf16", False, "bwd", 200),
+    ("s4096_b8_h2048_bf16", False, "bwd", 200),
+    ("s524288_b1_h384_bf16", False, "bwd", 100),
+    ("s8192_b4_h24576_bf16", False, "bwd", 40),
+    ("s16384_b32_h4096_fp16", True, "bwd", 20),
+    ("s16384_b32_h4096_fp16", False, "fwd", 40),
+]
+
+
+def run_extras(main_wl, main_inputs, dev, stream, peak):
+    """Times each EXTRAS entry with direct C-ABI calls (L2 flushed between
+    calls when a call moves less than four L2s) and returns one record each."""
+    import torch
+
+    import causal_conv_backward_gb300 as m
+    out = []
+    for name, no_mask, op, K in EXTRAS:
+        wl = workload(name, no_mask)
+        if wl.name == main_wl.name and op == "bwd":
+            continue
+        base = workload(name, False)
+        if base == main_wl:
+            d = dict(main_inputs)
+            if no_mask:
+                d["mask"] = None
+        else:
+            d, _ = device_inputs(wl, dev)
+        code = m.dtype_code(wl.dtype)
+        if op == "bwd":
+            gx = torch.empty_like(d["gy"])
+            gw = torch.empty_like(d["w"])
+            nb = m.mcc1d_bwd_workspace_size(wl.S, wl.B, wl.H, wl.W, code, d["mask"] is not None)
+            ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+            def step():
+                m.mcc1d_bwd(d["gy"], d["x"], d["w"], d["mask"], gx, gw, ws, stream, wl.S, wl.B, wl.H,
+                            wl.W, code, nb)
+            alg = wl.algorithmic_bytes()
+        else:
+            y = torch.empty_like(d["x"])
+
+            def step():
+                m.mcc1d_fwd(d["x"], d["w"], d["mask"], y, stream, wl.S, wl.B, wl.H, wl.W, code)
+            alg = wl.fwd_algorithmic_bytes()
+        flush = alg < 4 * L2_BYTES
+        flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize(dev)
+        per_call, _ = time_calls(step, K, stream, flush_buf)
+        med = statistics.median(per_call)
+        gbs = alg / med / 1e9
+        out.append({"workload": wl.name, "op": op, "calls": K,
+                    "l2": "flushed" if flush else "hot (inputs > 4x L2)",
+                    "median_call_ms": round(med * 1e3, 4), "GB/s": round(gbs, 1),
+                    "frac_of_copy_peak": round(gbs / peak, 4),
+                    "frac_of_spec_peak": round(gbs / SPEC_HBM_GBS, 4),
+                    "elements_per_s": float(f"{wl.E / med:.4e}"),
+                    "algorithmic_bytes": alg})
+        del d, flush_buf
+        torch.cuda.empty_cache()
+    return out
+
+
+def gpu_arm(args):
+    import torch
+
+    import causal_conv_backward_gb300 as m
     from causal_conv_backward_gb300 import build as cbuild
 
     rank, world, local = dist_env()
@@ -304,17 +453,8 @@ def gpu_arm(args):
 
     wl = chosen_workload(args)
     code = m.dtype_code(wl.dtype)
-
-    def pinned(shape, dt):
-        tdt = {np.uint16: torch.int16, np.uint8: torch.uint8}[dt]
-        return torch.empty(shape, dtype=tdt, pin_memory=True)
-
-    host = datagen.generate(wl, seed=0, alloc=pinned)
-    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
-    gy = host["gy"].to(dev).view(tdt)
-    x = host["x"].to(dev).view(tdt)
-    w = host["w"].to(dev).view(tdt)
-    mask = None if host["mask"] is None else host["mask"].to(dev)
+    d, host = device_inputs(wl, dev, pinned_host=True)
+    gy, x, w, mask = d["gy"], d["x"], d["w"], d["mask"]
     gx = torch.empty_like(gy)
     gw = torch.empty_like(w)
     nbytes = m.mcc1d_bwd_workspace_size(wl.S, wl.B, wl.H, 3, code, mask is not None)
@@ -356,8 +496,6 @@ def gpu_arm(args):
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if l2 == "flush" else None
     if flush_buf is not None and args.graph:
         raise SystemExit("bench.py: --graph times K calls back to back; it cannot flush L2 between them")
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     graph = None
     if args.graph:
         graph = torch.cuda.CUDAGraph()
@@ -371,25 +509,21 @@ def gpu_arm(args):
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.05)
-    start.record(stream)
     if graph is not None:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
         graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        elapsed = start.elapsed_time(end) / 1e3
+        per_call = [elapsed / K] * K
     else:
-        for k in range(K):
-            if flush_buf is not None:
-                flush_buf.fill_(k & 255)   # evict the previous call's lines from L2
-            ev[k][0].record(stream)
-            step()
-            ev[k][1].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+        per_call, elapsed = time_calls(step, K, stream, flush_buf)
     clocks = sampler.stop()
     barrier(dist, dev)
-    elapsed = start.elapsed_time(end) / 1e3
-    per_call = ([elapsed / K] * K if graph is not None
-                else [a.elapsed_time(b) / 1e3 for a, b in ev])
     if flush_buf is not None:
         elapsed = sum(per_call)   # the calls alone, without the flushes between them
+    del flush_buf
     t_max, bytes_all = aggregate(dist, elapsed, float(alg) * K, dev)
     value = bytes_all / t_max / 1e9
     tokens_h = float(wl.E) * K * world / t_max
@@ -426,6 +560,8 @@ def gpu_arm(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(te / n * 1e3, 3),
                "path": "mcc1d_bwd_host: pinned host tensors read and written in place by the kernel"}
+        del out_gx, out_gw
+    del host
 
     peak, peak_kind = measured_peak()
     avg_call = sum(per_call) / len(per_call)
@@ -436,12 +572,20 @@ def gpu_arm(args):
                 # bench workload (W = 3, dense [S,B,H]) only
                 "traffic": (profiled_traffic() if (args.op == "bwd" and wl.W == 3 and args.layout == "sbh"
                                                    and wl == workload(WORKLOAD, False)) else None),
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: a 1:1 copy)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
+                "frac_of_spec_peak": round(achieved / SPEC_HBM_GBS, 4),
+                "spec_peak": SPEC_HBM_GBS,
                 "kernel": ("mcc1d_bwd_main (timed as the whole call: main + reduce)" if args.op == "bwd"
                            else "mcc1d_fwd_main"),
                 "algorithmic_bytes_per_launch": alg,
                 "median_call_ms": round(statistics.median(per_call) * 1e3, 4)}
+
+    extras = None
+    if rank == 0 and world == 1 and not args.no_extras and args.layout == "sbh" and wl.W == 3 \
+            and not args.seq_len:
+        # inputs of the headline workload stay resident; the output buffers go
+        extras = run_extras(wl, d, dev, stream, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.op == "bwd":
@@ -458,12 +602,14 @@ def gpu_arm(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": f"synthetic (seeded generator; {wl.dtype} bit patterns)",
             "config": describe(wl, args.layout, l2, alg), "tokens_h_per_s": float(f"{tokens_h:.4e}"),
-            "frac_of_peak": round(value / world / peak, 4),
+            "frac_of_copy_peak": round(value / world / peak, 4),
+            "frac_of_spec_peak": round(value / world / SPEC_HBM_GBS, 4),
             "op": args.op,
             "e2e": e2e, "gpu_launches": (2 if args.op == "bwd" else 1) * K, "roofline": roofline,
             "cpu_baseline": cpu,
             "timing": "one CUDA graph of K calls" if graph is not None else "K direct C-ABI calls",
             "clocks": clocks,
+            "workloads": extras,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -495,10 +641,15 @@ def reference_arm(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
-        reference_arm(args)
-    else:
-        gpu_arm(args)
+    target = reference_arm if args.impl == "reference" else gpu_arm
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not launched by torch.distributed.run: start the N replicas here
+        if args.impl != "reference":
+            import torch
+            if torch.cuda.device_count() < args.gpus:
+                raise SystemExit(f"bench.py: --gpus {args.gpus} but {torch.cuda.device_count()} GPUs visible")
+        sys.exit(spawn_replicas(args.gpus, target, args))
+    target(args)
 
 
 if __name__ == "__main__":

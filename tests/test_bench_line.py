@@ -48,7 +48,7 @@ def test_cuda_arm_line():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    d = run_bench("--steps", "5", "--warmup", "3", "--workload", "s4096_b8_h2048_bf16")
+    d = run_bench("--steps", "5", "--warmup", "3", "--workload", "s4096_b8_h2048_bf16", "--no-extras")
     check_base(d)
     rf = d["roofline"]
     for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
