@@ -244,7 +244,7 @@ int32_t fwd_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan
     st = make_plan_for(S, B, H, W, dtype, o, p);
     if (st != kOk)
         return st;
-    o.regs_bound = fwd_kernel_regs(p->dtype, p->vec, p->W);
+    o.regs_bound = fwd_kernel_regs(p->dtype, p->vec, p->W, fwd_bulk_store(*p));
     if (o.regs_bound > 0)
         st = make_plan_for(S, B, H, W, dtype, o, p);
     return st;

@@ -278,30 +278,10 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                 uint32_t o[NP];
 #pragma unroll
                 for (int e = 0; e < NP; ++e) {
-                    // gradX = sum_k gYm(i+k) w(W-1-k). Products of two 16-bit
-                    // values are exact in fp32; a TwoSum cascade keeps every
-                    // rounding error but the last add's, then adds them back:
-                    // within a hair of the exact sum (for W = 3: TwoSum of the
-                    // first two products, one more add, the correction).
-                    float2 pk[W];
-#pragma unroll
-                    for (int k = 0; k < W; ++k)
-                        pk[k] = mul2(k < WH ? win[k].e[e] : gn.e[e], wt[W - 1 - k].e[e]);
-                    float2 s = pk[0], err = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int k = 1; k < W - 1; ++k) {
-                        const float2 sn = add2(s, pk[k]);
-                        const float2 bb = sub2(sn, s);
-                        const float2 ek = add2(sub2(s, sub2(sn, bb)), sub2(pk[k], bb));
-                        err = (k == 1) ? ek : add2(err, ek);
-                        s = sn;
-                    }
-                    if (W >= 3)
-                        o[e] = pack2<DT>(add2(add2(s, pk[W - 1]), err));
-                    else if (W == 2)
-                        o[e] = pack2<DT>(add2(s, pk[1]));
-                    else
-                        o[e] = pack2<DT>(s);
+                    // gradX = sum_k gYm(i+k) w(W-1-k): exact fp32 products,
+                    // a compensated sum, rounded once (sum_to16)
+                    o[e] = sum_to16<DT, W>(
+                        [&](int k) { return mul2(k < WH ? win[k].e[e] : gn.e[e], wt[W - 1 - k].e[e]); });
                     // gradWeight tap k pairs x(i) with gYm(i+W-1-k)
 #pragma unroll
                     for (int k = 0; k < W; ++k)
@@ -384,6 +364,11 @@ __device__ __forceinline__ void main_body(const MainParams &p)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
+    // Launched as a programmatic dependent of whatever precedes it on the
+    // stream (the previous call's reduce, typically): the set-up above may
+    // overlap that kernel's tail, but no global memory is touched before it
+    // has completed and its writes are visible. A no-op otherwise.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int lane = threadIdx.x & 31;
     bool dead;

@@ -148,7 +148,7 @@ template <int NP>
 __device__ __forceinline__ Raw<NP> load_raw(const void *p)
 {
     Raw<NP> r;
-    if (NP == 4) {
+    if constexpr (NP == 4) {
         const uint4 v = *reinterpret_cast<const uint4 *>(p);
         r.u[0] = v.x;
         r.u[1] = v.y;
@@ -167,7 +167,7 @@ template <int NP>
 __device__ __forceinline__ Raw<NP> ldg_raw(const void *p)
 {
     Raw<NP> r;
-    if (NP == 4) {
+    if constexpr (NP == 4) {
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
         r.u[0] = v.x;
         r.u[1] = v.y;
@@ -185,7 +185,7 @@ __device__ __forceinline__ Raw<NP> ldg_raw(const void *p)
 template <int NP>
 __device__ __forceinline__ void store_cs(void *p, const uint32_t (&u)[NP])
 {
-    if (NP == 4)
+    if constexpr (NP == 4)
         __stcs(reinterpret_cast<uint4 *>(p), make_uint4(u[0], u[1], u[2], u[3]));
     else
         __stcs(reinterpret_cast<uint2 *>(p), make_uint2(u[0], u[1]));
@@ -212,6 +212,38 @@ __device__ __forceinline__ Vf<NP> load_masked(const uint8_t *p, uint8_t keep_byt
     for (int e = 0; e < NP; ++e)
         r.u[e] &= keep;
     return unpack<DT, NP>(r);
+}
+
+// ------------------------------------------------------------------ sums of W products
+// The gradX (and forward y) value of a channel is a sum of W products of two
+// 16-bit values. Each product is exact in fp32 (8 x 8 or 11 x 11 significant
+// bits), so only the additions round. A TwoSum cascade over the first W-1
+// products keeps every rounding error, the last product is added plainly,
+// then the summed errors: within a hair of the exact sum, rounded once to
+// the 16-bit type (W = 3: TwoSum of the first two, one more add, the
+// correction). prod(k) returns product k for two channels.
+template <int DT, int W, typename Prod>
+__device__ __forceinline__ uint32_t sum_to16(Prod prod)
+{
+    float2 pk[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+        pk[k] = prod(k);
+    float2 s = pk[0], err = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 1; k < W - 1; ++k) {
+        const float2 sn = add2(s, pk[k]);
+        const float2 bb = sub2(sn, s);
+        const float2 ek = add2(sub2(s, sub2(sn, bb)), sub2(pk[k], bb));
+        err = (k == 1) ? ek : add2(err, ek);
+        s = sn;
+    }
+    if constexpr (W >= 3)
+        return pack2<DT>(add2(add2(s, pk[W - 1]), err));
+    else if constexpr (W == 2)
+        return pack2<DT>(add2(s, pk[1]));
+    else
+        return pack2<DT>(s);
 }
 
 // ------------------------------------------------------------------ row cursor

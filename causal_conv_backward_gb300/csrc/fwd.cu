@@ -11,10 +11,17 @@
 //
 // Same streaming design as the backward, with the W-1-row halo behind each
 // row instead of ahead: per stage the producer warp copies x rows t .. t+R-1
-// (plus t-(W-1) .. t-1 when a sequence or CTA range starts) into a ring slot
-// with cp.async.bulk and stores the stage's output-mask bytes; consumer
-// threads keep the last W-1 x rows in registers, form y with the compensated
-// W-term sum and a streaming store. No reduction, no workspace.
+// into a ring slot with cp.async.bulk and stores the stage's output-mask
+// bytes; consumer threads keep the last W-1 x rows in registers, form y with
+// the compensated W-term sum and a streaming store. The halo rows
+// t-(W-1) .. t-1 are real data only at the first stage of a CTA range that
+// starts inside a sequence (at a sequence start they are the zero padding):
+// they go to a separate W-1-row area once, so the slots hold output rows
+// only and the ring holds more stages. With 4 KB rows the consumers write
+// each y row back into the slot row it was read from and one thread stores
+// the stage's rows with bulk copies (shared -> global), so y leaves in whole
+// rows like x arrives; narrower rows keep per-thread streaming stores. No
+// reduction, no workspace.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -32,6 +39,11 @@ namespace mcc1d {
 constexpr int kFwdR = 8;             // output rows per stage
 constexpr int kFwdMaxThreads = 288;  // 8 consumer warps + producer
 constexpr int kFwdMaxStages = 8;
+// 4 KB rows: two ring slots per CTA (more measured slower on this 1:1
+// read/write stream), and over long CTA ranges y leaves by bulk copies
+constexpr uint32_t kFwdWideRowBytes = 4096;
+constexpr int kFwdWideMaxStages = 2;
+constexpr int64_t kFwdBulkStoreMinRowsPerCta = 1024;
 
 struct FwdParams {
     const uint8_t *x;      // [S,B,H] 16-bit, addressed in bytes
@@ -41,13 +53,20 @@ struct FwdParams {
     int32_t *status;       // device word or null: set to kErrTimeout if a wait gives up
     int64_t S, BS, H, N;
     int32_t B, hb_width, ncta, stages;
-    uint32_t row_bytes, slot_bytes, off_mask, off_bar;
+    uint32_t row_bytes, slot_bytes, off_halo, off_mask, off_bar;
     int32_t contig_rows;
     // Input strides (elements; mask bytes); x has unit H stride and 16-byte
     // aligned rows (other layouts are gathered into a dense copy first).
     int64_t x_s, x_b, w_k, w_h, m_b, m_s;
     int32_t w_vec;         // weight rows can be read as aligned vectors
 };
+
+// Shared -> global bulk copy of one row, in the thread's bulk-async group.
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
 
 // Byte q of a stage (row cursor at output row t = c.i): q < W-1 says whether
 // the halo row t-(W-1)+q exists (is >= 0); q >= W-1 is the output mask of row
@@ -101,24 +120,33 @@ __device__ bool fwd_produce(const FwdParams &p, uint8_t *smem, int64_t r0, int64
         const int64_t hb0 = (int64_t)cur.hb * p.hb_width;
         const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
         const uint32_t wbytes = (uint32_t)width * 2u;
-        // slot row q holds x row t-(W-1)+q; the stage loads q in [q0, n+W-1)
-        int q0 = W - 1;
-        if (head)
-            q0 = cur.i >= W - 1 ? 0 : (int)(W - 1 - cur.i);
-        const int nrows = n + W - 1 - q0;
+        // slot row r holds x row t+r (r < n); halo row q holds x row
+        // t-(W-1)+q, loaded for q in [h0, W-1) at the first stage of a range
+        // that starts inside a sequence, never again
+        int h0 = W - 1;
+        if (stage == 0 && cur.i > 0)
+            h0 = cur.i >= W - 1 ? 0 : (int)(W - 1 - cur.i);
+        const int nh = W - 1 - h0;
         __syncwarp();
         if (lane == 0)
-            mbar_arrive_expect_tx(bar_full0 + 8u * slot, (uint32_t)nrows * wbytes);
+            mbar_arrive_expect_tx(bar_full0 + 8u * slot, (uint32_t)(nh + n) * wbytes);
         __syncwarp();
         const uint32_t slot_base = ring0 + (uint32_t)slot * p.slot_bytes;
+        const uint32_t halo_base = ring0 + p.off_halo;
         if (p.contig_rows) {
-            if (lane == 0)
-                bulk_g2s(slot_base + (uint32_t)q0 * p.row_bytes, p.x + 2 * (cur.i - (W - 1) + q0) * p.x_s,
-                         (uint32_t)nrows * wbytes, bar_full0 + 8u * slot);
-        } else if (lane < nrows) {
-            const int q = q0 + lane;
+            if (lane == 0) {
+                bulk_g2s(slot_base, p.x + 2 * cur.i * p.x_s, (uint32_t)n * wbytes, bar_full0 + 8u * slot);
+                if (nh > 0)
+                    bulk_g2s(halo_base + (uint32_t)h0 * p.row_bytes, p.x + 2 * (cur.i - (W - 1) + h0) * p.x_s,
+                             (uint32_t)nh * wbytes, bar_full0 + 8u * slot);
+            }
+        } else if (lane < n) {
+            const int64_t e = (cur.i + lane) * p.x_s + (int64_t)cur.j * p.x_b + hb0;
+            bulk_g2s(slot_base + (uint32_t)lane * p.row_bytes, p.x + 2 * e, wbytes, bar_full0 + 8u * slot);
+        } else if (lane < n + nh) {
+            const int q = h0 + lane - n;
             const int64_t e = (cur.i - (W - 1) + q) * p.x_s + (int64_t)cur.j * p.x_b + hb0;
-            bulk_g2s(slot_base + (uint32_t)q * p.row_bytes, p.x + 2 * e, wbytes, bar_full0 + 8u * slot);
+            bulk_g2s(halo_base + (uint32_t)q * p.row_bytes, p.x + 2 * e, wbytes, bar_full0 + 8u * slot);
         }
         cur.advance(n, p.S, p.B);
         ++stage;
@@ -153,7 +181,7 @@ __device__ __forceinline__ Vf<NP> fwd_weight(const FwdParams &p, int k, int64_t 
     return unpack<DT, NP>(r);
 }
 
-template <int DT, int R, int NP, int W>
+template <int DT, int R, int NP, int W, bool BS>
 __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64_t r1, int ct, int lane)
 {
     constexpr int CH = 2 * NP;
@@ -196,48 +224,39 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             dead = __any_sync(0xFFFFFFFFu, !ok);
         }
         if (!dead && active) {
-            const uint8_t *xs = smem + (size_t)slot * p.slot_bytes + 2 * CH * ct;
+            uint8_t *xs = smem + (size_t)slot * p.slot_bytes + 2 * CH * ct;
             const uint8_t *ms = smem + p.off_mask + 32u * slot;
             if (head) {
+                // halo rows: staged at a range's first stage, zero (mask
+                // byte 0) at a sequence start
+                const uint8_t *hs = smem + p.off_halo + 2 * CH * ct;
 #pragma unroll
                 for (int q = 0; q < WH; ++q)
-                    win[q] = load_masked<DT, NP>(xs + (size_t)q * p.row_bytes, ms[q]);
+                    win[q] = load_masked<DT, NP>(hs + (size_t)q * p.row_bytes, ms[q]);
             }
             uint8_t *yp = p.y + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
             auto row = [&](int r) {
-                const Vf<NP> xn = unpack<DT, NP>(load_raw<NP>(xs + (size_t)(r + WH) * p.row_bytes));
+                const Vf<NP> xn = unpack<DT, NP>(load_raw<NP>(xs + (size_t)r * p.row_bytes));
                 const uint32_t keep = 0u - (uint32_t)ms[r + WH];
                 uint32_t o[NP];
 #pragma unroll
                 for (int e = 0; e < NP; ++e) {
-                    // products of two 16-bit values are exact in fp32; a TwoSum
-                    // cascade over the first W-1 keeps every rounding error,
-                    // the last product is added plainly, then the errors
-                    // (W = 3: TwoSum of the first two, one more add, the
-                    // correction)
-                    float2 pk[W];
-#pragma unroll
-                    for (int k = 0; k < W; ++k)
-                        pk[k] = mul2(k < WH ? win[k].e[e] : xn.e[e], wt[k].e[e]);
-                    float2 s = pk[0], err = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int k = 1; k < W - 1; ++k) {
-                        const float2 sn = add2(s, pk[k]);
-                        const float2 bb = sub2(sn, s);
-                        const float2 ek = add2(sub2(s, sub2(sn, bb)), sub2(pk[k], bb));
-                        err = (k == 1) ? ek : add2(err, ek);
-                        s = sn;
-                    }
-                    float2 t;
-                    if (W >= 3)
-                        t = add2(add2(s, pk[W - 1]), err);
-                    else if (W == 2)
-                        t = add2(s, pk[1]);
-                    else
-                        t = s;
-                    o[e] = pack2<DT>(t) & keep;  // output mask
+                    // exact fp32 products, summed and rounded once by
+                    // sum_to16 (the backward's gradX sum)
+                    o[e] = sum_to16<DT, W>(
+                               [&](int k) { return mul2(k < WH ? win[k].e[e] : xn.e[e], wt[k].e[e]); }) &
+                           keep;  // output mask
                 }
-                store_cs<NP>(yp + (int64_t)r * row_stride, o);
+                if constexpr (BS) {
+                    // x(t+r) was read from this slot row above and now lives
+                    // in the register window: the row takes y(t+r) instead
+                    if constexpr (NP == 4)
+                        *reinterpret_cast<uint4 *>(xs + (size_t)r * p.row_bytes) = make_uint4(o[0], o[1], o[2], o[3]);
+                    else
+                        *reinterpret_cast<uint2 *>(xs + (size_t)r * p.row_bytes) = make_uint2(o[0], o[1]);
+                } else {
+                    store_cs<NP>(yp + (int64_t)r * row_stride, o);
+                }
 #pragma unroll
                 for (int q = 0; q + 1 < WH; ++q)
                     win[q] = win[q + 1];
@@ -255,9 +274,28 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                         row(r);
             }
         }
-        __syncwarp();
-        if (!dead && lane == 0)
-            mbar_arrive(bar_empty0 + 8u * slot);
+        if constexpr (BS) {
+            // every consumer's y values of the stage are in the slot (their
+            // writes made visible to the bulk-copy engine); one thread stores
+            // the rows, and releases the slot once the copies have read it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"r"((int)blockDim.x - 32) : "memory");
+            if (ct == 0 && !dead) {
+                const int64_t hb0 = (int64_t)cur.hb * p.hb_width;
+                const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
+                const uint32_t sbase = smem_u32(smem + (size_t)slot * p.slot_bytes);
+                for (int r = 0; r < n; ++r)
+                    bulk_s2g(p.y + 2 * (((cur.i + r) * p.B + cur.j) * p.H + hb0), sbase + (uint32_t)r * p.row_bytes,
+                             (uint32_t)width * 2u);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                mbar_arrive(bar_empty0 + 8u * slot);
+            }
+        } else {
+            __syncwarp();
+            if (!dead && lane == 0)
+                mbar_arrive(bar_empty0 + 8u * slot);
+        }
         cur.advance(n, p.S, p.B);
         ++stage;
         if (++slot == NS) {
@@ -265,10 +303,12 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             ph ^= 1u;
         }
     }
+    if (BS && ct == 0)
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the y rows are written
     return dead;
 }
 
-template <int DT, int R, int NP, int W>
+template <int DT, int R, int NP, int W, bool BS>
 __device__ __forceinline__ void fwd_body(const FwdParams &p)
 {
     // one producer lane per staged row, and the stage's flag bytes fit the
@@ -285,18 +325,23 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         const uint32_t bar0 = smem_u32(smem + p.off_bar);
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(bar0 + 8u * s, 1);
-            mbar_init(bar0 + 8u * (p.stages + s), (uint32_t)consumer_warps);
+            mbar_init(bar0 + 8u * (p.stages + s), BS ? 1u : (uint32_t)consumer_warps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
+    // a programmatic dependent of the preceding kernel: the set-up above may
+    // overlap its tail; memory is touched only after it has completed. The
+    // next kernel may start its own set-up now.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     bool dead;
     if (threadIdx.x < 32)
         dead = fwd_produce<R, W>(p, smem, r0, r1, lane);
     else
-        dead = fwd_consume<DT, R, NP, W>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
+        dead = fwd_consume<DT, R, NP, W, BS>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
     if (dead && lane == 0)
         atomicOr(&s_err, 1);
     __syncthreads();
@@ -304,10 +349,12 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         atomicOr(p.status, kErrTimeout);
 }
 
-template <int DT, int R, int NP, int W>
-__global__ void __launch_bounds__(kFwdMaxThreads) mcc1d_fwd_main(const __grid_constant__ FwdParams p)
+// Held to the registers that let two CTAs share an SM (96), so the plan's
+// register cap keeps two of them per SM.
+template <int DT, int R, int NP, int W, bool BS>
+__global__ void __launch_bounds__(kFwdMaxThreads, 2) mcc1d_fwd_main(const __grid_constant__ FwdParams p)
 {
-    fwd_body<DT, R, NP, W>(p);
+    fwd_body<DT, R, NP, W, BS>(p);
 }
 
 // The same kernel compiled for one CTA per SM, for the widest kernels, whose
@@ -315,83 +362,97 @@ __global__ void __launch_bounds__(kFwdMaxThreads) mcc1d_fwd_main(const __grid_co
 template <int DT, int R, int NP, int W>
 __global__ void __launch_bounds__(kFwdMaxThreads, 1) mcc1d_fwd_main_1(const __grid_constant__ FwdParams p)
 {
-    fwd_body<DT, R, NP, W>(p);
+    fwd_body<DT, R, NP, W, false>(p);
 }
 
 typedef void (*FwdFn)(FwdParams);
 
-// W = 3 (the page's width) with 8 or 4 channels per thread; other widths with
-// 4 (their plan keeps H-blocks of at most 1024 channels), from W = 6 in the
-// one-CTA form.
+// W = 3 (the page's width) with 8 or 4 channels per thread, its 4 KB rows
+// (8 channels per thread) with bulk stores; other widths with 4 channels per
+// thread (their plan keeps H-blocks of at most 1024 channels), from W = 6 in
+// the one-CTA form.
 template <int DT, int W>
-static FwdFn fwd_pick(int vec)
+static FwdFn fwd_pick(int vec, bool bulk)
 {
-    if constexpr (W == 3)
-        return vec == 4 ? mcc1d_fwd_main<DT, kFwdR, 2, 3> : mcc1d_fwd_main<DT, kFwdR, 4, 3>;
-    else if constexpr (W >= 6)
-        return vec == 4 ? mcc1d_fwd_main_1<DT, kFwdR, 2, W> : nullptr;
-    else
-        return vec == 4 ? mcc1d_fwd_main<DT, kFwdR, 2, W> : nullptr;
+    if constexpr (W == 3) {
+        if (vec == 4)
+            return bulk ? nullptr : mcc1d_fwd_main<DT, kFwdR, 2, 3, false>;
+        return bulk ? mcc1d_fwd_main<DT, kFwdR, 4, 3, true> : mcc1d_fwd_main<DT, kFwdR, 4, 3, false>;
+    } else if constexpr (W >= 6) {
+        return vec == 4 && !bulk ? mcc1d_fwd_main_1<DT, kFwdR, 2, W> : nullptr;
+    } else {
+        return vec == 4 && !bulk ? mcc1d_fwd_main<DT, kFwdR, 2, W, false> : nullptr;
+    }
 }
 
 template <int DT>
-static FwdFn fwd_pick_w(int vec, int W)
+static FwdFn fwd_pick_w(int vec, int W, bool bulk)
 {
     switch (W) {
-    case 1: return fwd_pick<DT, 1>(vec);
-    case 2: return fwd_pick<DT, 2>(vec);
-    case 3: return fwd_pick<DT, 3>(vec);
-    case 4: return fwd_pick<DT, 4>(vec);
-    case 5: return fwd_pick<DT, 5>(vec);
-    case 6: return fwd_pick<DT, 6>(vec);
-    case 7: return fwd_pick<DT, 7>(vec);
-    case 8: return fwd_pick<DT, 8>(vec);
+    case 1: return fwd_pick<DT, 1>(vec, bulk);
+    case 2: return fwd_pick<DT, 2>(vec, bulk);
+    case 3: return fwd_pick<DT, 3>(vec, bulk);
+    case 4: return fwd_pick<DT, 4>(vec, bulk);
+    case 5: return fwd_pick<DT, 5>(vec, bulk);
+    case 6: return fwd_pick<DT, 6>(vec, bulk);
+    case 7: return fwd_pick<DT, 7>(vec, bulk);
+    case 8: return fwd_pick<DT, 8>(vec, bulk);
     default: return nullptr;
     }
 }
 
-static FwdFn fwd_kernel(int dtype, int vec, int W)
+static FwdFn fwd_kernel(int dtype, int vec, int W, bool bulk)
 {
-    return dtype == 0 ? fwd_pick_w<0>(vec, W) : fwd_pick_w<1>(vec, W);
+    return dtype == 0 ? fwd_pick_w<0>(vec, W, bulk) : fwd_pick_w<1>(vec, W, bulk);
+}
+
+bool fwd_bulk_store(const Plan &pl)
+{
+    return pl.W == 3 && pl.vec == 8 && pl.row_bytes >= kFwdWideRowBytes && long_ranges(pl) &&
+           pl.rows_total / pl.ncta >= kFwdBulkStoreMinRowsPerCta;
 }
 
 FwdRing fwd_ring(const Plan &pl)
 {
-    // kFwdR output rows plus the W-1 halo rows per slot; as many slots as the
-    // CTA's share of shared memory allows, 2 .. kFwdMaxStages
+    // kFwdR output rows per slot, one W-1-row halo area; as many slots as
+    // the CTA's share of shared memory allows, 2 .. kFwdMaxStages
     FwdRing r;
     r.rows_per_stage = kFwdR;
-    r.slot_bytes = (uint32_t)(kFwdR + pl.W - 1) * pl.row_bytes;
+    r.slot_bytes = (uint32_t)kFwdR * pl.row_bytes;
+    const uint32_t halo_bytes = (uint32_t)(pl.W - 1) * pl.row_bytes;
     int64_t budget = kSmemPerSM / pl.ctas_per_sm - kSmemReservedPerCta;
     if (budget > kSmemDynMax)
         budget = kSmemDynMax;
-    budget -= 64;
+    budget -= 64 + halo_bytes;
     int64_t ns = budget / (r.slot_bytes + 48);
     if (ns > kFwdMaxStages)
         ns = kFwdMaxStages;
+    if (pl.row_bytes >= kFwdWideRowBytes && ns > kFwdWideMaxStages)
+        ns = kFwdWideMaxStages;
     if (ns < 2)
         ns = 2;
     r.stages = (int32_t)ns;
-    r.off_mask = (uint32_t)ns * r.slot_bytes;
+    r.off_halo = (uint32_t)ns * r.slot_bytes;
+    r.off_mask = r.off_halo + halo_bytes;
     r.off_bar = (r.off_mask + 32u * (uint32_t)ns + 15u) & ~15u;
     r.smem_bytes = r.off_bar + 16u * (uint32_t)ns;
     return r;
 }
 
-int fwd_kernel_regs(int dtype, int vec, int W)
+int fwd_kernel_regs(int dtype, int vec, int W, bool bulk)
 {
     // registers per thread of the forward instance (cached per device and
     // instance; 0 when the runtime cannot say)
-    static std::atomic<int> cache[64][4 * (kMaxW + 1)];
+    static std::atomic<int> cache[64][8 * (kMaxW + 1)];
     if (W < 1 || W > kMaxW)
         return 0;
-    const FwdFn fn = fwd_kernel(dtype, vec, W);
+    const FwdFn fn = fwd_kernel(dtype, vec, W, bulk);
     if (fn == nullptr)
         return 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 0;
-    const int slot = (dtype * 2 + (vec == 4 ? 1 : 0)) * (kMaxW + 1) + W;
+    const int slot = ((dtype * 2 + (vec == 4 ? 1 : 0)) * 2 + (bulk ? 1 : 0)) * (kMaxW + 1) + W;
     std::atomic<int> &c = cache[dev & 63][slot];
     int r = c.load(std::memory_order_acquire);
     if (r > 0)
@@ -423,6 +484,7 @@ int32_t launch_fwd(const Plan &pl, const Layout &L, const void *x, const void *w
     fp.row_bytes = pl.row_bytes;
     const FwdRing ring = fwd_ring(pl);
     fp.slot_bytes = ring.slot_bytes;
+    fp.off_halo = ring.off_halo;
     fp.stages = ring.stages;
     fp.off_mask = ring.off_mask;
     fp.off_bar = ring.off_bar;
@@ -436,13 +498,14 @@ int32_t launch_fwd(const Plan &pl, const Layout &L, const void *x, const void *w
     fp.w_vec = (L.w[1] == 1 && (L.w[0] * 2) % 16 == 0 && ((uintptr_t)weight & 15u) == 0) ? 1 : 0;
     fp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && L.x[0] == pl.H && !long_ranges(pl)) ? 1 : 0;
 
-    FwdFn fn = fwd_kernel(pl.dtype, pl.vec, pl.W);
+    const bool bulk = fwd_bulk_store(pl);
+    FwdFn fn = fwd_kernel(pl.dtype, pl.vec, pl.W, bulk);
     if (fn == nullptr)
         return kErrCuda;
     // the shared-memory attribute, once per (instance, device, context): a
     // context created after a device reset starts without it
-    static std::atomic<unsigned long long> done[4 * (kMaxW + 1)][64];
-    const int slot_id = (pl.dtype * 2 + (pl.vec == 4 ? 1 : 0)) * (kMaxW + 1) + pl.W;
+    static std::atomic<unsigned long long> done[8 * (kMaxW + 1)][64];
+    const int slot_id = ((pl.dtype * 2 + (pl.vec == 4 ? 1 : 0)) * 2 + (bulk ? 1 : 0)) * (kMaxW + 1) + pl.W;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return kErrCuda;
@@ -454,11 +517,16 @@ int32_t launch_fwd(const Plan &pl, const Layout &L, const void *x, const void *w
             return kErrCuda;
         done[slot_id][dev].store(ctx != 0 ? ctx : current_context_id(), std::memory_order_release);
     }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.ncta);
     cfg.blockDim = dim3((unsigned)pl.threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, fn, fp) != cudaSuccess)
         return kErrCuda;
     return kOk;

@@ -65,6 +65,9 @@ template <int DT>
 __global__ void __launch_bounds__(kReduceThreads) mcc1d_bwd_reduce(const __grid_constant__ ReduceParams p)
 {
     __shared__ float4 red[kReduceThreads];   // [split][lane]
+    // the next call's main kernel may start its set-up now; it waits for
+    // this grid's completion before it touches memory
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lanes = 1 << p.lanes_log2;
     const int lane = threadIdx.x & (lanes - 1), split = threadIdx.x >> p.lanes_log2;
@@ -322,9 +325,15 @@ int32_t launch_bwd(const Plan &pl, const Layout &L, const void *gradY, const voi
     cfg.blockDim = dim3((unsigned)pl.threads);
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = stream;
+    // a programmatic dependent of the preceding kernel (the kernel waits for
+    // it before touching memory)
+    cudaLaunchAttribute cattr[1];
+    cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    cattr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = cattr;
+    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, mfn, mp) != cudaSuccess)
         return kErrCuda;
-
     return launch_reduce(pl, workspace, gradWeight, stream);
 }
 

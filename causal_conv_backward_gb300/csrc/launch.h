@@ -37,16 +37,19 @@ int32_t launch_pack(const void *src, const int64_t strides[3], void *dst, int64_
 // depth; the backward's ring fields of the plan do not apply to it).
 struct FwdRing {
     int32_t rows_per_stage, stages;
-    uint32_t slot_bytes, off_mask, off_bar, smem_bytes;
+    uint32_t slot_bytes, off_halo, off_mask, off_bar, smem_bytes;
 };
 FwdRing fwd_ring(const Plan &p);
+// Whether the forward stores y rows with bulk copies out of its ring (wide
+// rows) rather than with per-thread stores.
+bool fwd_bulk_store(const Plan &p);
 // One thread waiting on an mbarrier with the library's bounded wait; writes
 // kOk (arrive != 0: it arrives first) or kErrTimeout (nothing arrives) to the
 // device word `status`.
 int32_t launch_wait_selftest(int32_t *status, int32_t arrive, cudaStream_t stream);
-// Registers per thread of the forward kernel instance for (dtype, vec, W),
-// from the runtime (0 when unknown).
-int fwd_kernel_regs(int dtype, int vec, int W);
+// Registers per thread of the forward kernel instance for (dtype, vec, W,
+// bulk stores), from the runtime (0 when unknown).
+int fwd_kernel_regs(int dtype, int vec, int W, bool bulk);
 // Enqueues the forward kernel of plan `p`; the inputs are read with layout L
 // (x with unit H stride and 16-byte aligned rows), y is dense. `status` is a
 // device word the kernel ORs kErrTimeout into if a wait gives up, or null.

@@ -123,23 +123,35 @@ def model_forward(S, B, H, W, full):
     cw = p["consumer_warps"]
     contig = B == 1 and p["n_hb"] == 1 and p["rows_total"] // p["ncta"] < KDEEP
     written = np.zeros(E // vec, np.int32) if full else None
+    halo = (W - 1) * rb
+    bulk = W == 3 and vec == 8 and rb >= 4096 and p["rows_total"] // p["ncta"] >= 1024
     for c in ctas_to_check(p["ncta"], full):
         for stage, i, j, hb, n in walk(p, c):
-            head = stage == 0 or i == 0
             hb0 = hb * hbw
             width = min(hbw, H - hb0)
             wbytes = 2 * width
-            # slot row q holds x row i-(W-1)+q; the stage loads q in [q0, n+W-1)
-            q0 = W - 1
-            if head:
-                q0 = 0 if i >= W - 1 else W - 1 - i
-            nrows = n + W - 1 - q0
-            assert nrows <= 32
+            # slot row r holds x row i+r (r < n); halo row q holds x row
+            # i-(W-1)+q, loaded for q in [h0, W-1) at a range's first stage
+            # when it starts inside a sequence
+            h0 = W - 1
+            if stage == 0 and i > 0:
+                h0 = 0 if i >= W - 1 else W - 1 - i
+            nh = W - 1 - h0
+            assert n + nh <= 32
             if contig:
-                check_copy((i - (W - 1) + q0) * H, nrows * wbytes, E, q0 * rb, sb)
+                check_copy(i * H, n * wbytes, E, 0, sb)
+                if nh:
+                    check_copy((i - (W - 1) + h0) * H, nh * wbytes, E, h0 * rb, halo)
             else:
-                for q in range(q0, n + W - 1):
-                    check_copy((i - (W - 1) + q) * B * H + j * H + hb0, wbytes, E, q * rb, sb)
+                for r in range(n):
+                    check_copy((i + r) * B * H + j * H + hb0, wbytes, E, r * rb, sb)
+                for q in range(h0, W - 1):
+                    check_copy((i - (W - 1) + q) * B * H + j * H + hb0, wbytes, E, q * rb, halo)
+            if bulk:
+                # y rows leave from the slot rows they were read into, one bulk
+                # copy (shared -> global) per row
+                for r in range(n):
+                    check_copy((i + r) * B * H + j * H + hb0, wbytes, E, r * rb, sb)
             ct = np.arange(cw * 32)
             ct = ct[vec * ct < width]
             for r in range(n):
@@ -192,3 +204,4 @@ def test_random_shapes_model():
         W = int(rng.integers(1, 9))
         model_backward(S, B, H, W, m.PLAN_BWD_EX, full=True)
         model_forward(S, B, H, W, full=True)
+

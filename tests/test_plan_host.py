@@ -47,7 +47,7 @@ def check_common(p, S, B, H, W):
     assert cps >= 1 and cps * p["threads"] <= 2048
     assert p["smem_bytes"] <= SMEM_PER_CTA_DYN
     assert cps * (p["smem_bytes"] + RESERVED_PER_CTA) <= SMEM_PER_SM
-    assert p["off_mask"] == p["stages"] * p["slot_bytes"]
+    assert p["off_mask"] >= p["stages"] * p["slot_bytes"]
     assert p["off_bar"] >= p["off_mask"] + 32 * p["stages"] and p["off_bar"] % 16 == 0
     # CTA ranges: every row of every H-block in exactly one range, ranges
     # contiguous (CTA c starts at c * rows // ncta)
@@ -66,11 +66,13 @@ def check_common(p, S, B, H, W):
 
 def check_bwd(p, S, B, H, W):
     check_common(p, S, B, H, W)
+    assert W < 4 or (p["vec"] == 4 and p["hb_width"] <= 1024)
     R = p["rows_per_stage"]
     assert R in ((4, 6, 8, 14) if W == 3 else (6,))
     assert R != 14 or p["vec"] == 4
     assert 2 * R + W - 1 <= 32               # one producer lane per staged row
     assert p["slot_bytes"] == (2 * R + W - 1) * p["row_bytes"]
+    assert p["off_mask"] == p["stages"] * p["slot_bytes"]
     assert p["off_outer"] >= p["off_bar"] + 16 * p["stages"] and p["off_outer"] % 16 == 0
     assert p["smem_bytes"] == p["off_outer"] + p["consumer_warps"] * 32 * W * p["vec"] * 4
     # registers: CTAs per SM within the register file at the kernel's bound
@@ -95,7 +97,9 @@ def check_bwd(p, S, B, H, W):
 def check_fwd(p, S, B, H, W=3):
     check_common(p, S, B, H, W)
     assert p["rows_per_stage"] + W - 1 <= 32       # one producer lane per staged row
-    assert p["slot_bytes"] == (p["rows_per_stage"] + W - 1) * p["row_bytes"]
+    # slots hold output rows only; one W-1-row halo area follows the slots
+    assert p["slot_bytes"] == p["rows_per_stage"] * p["row_bytes"]
+    assert p["off_mask"] == p["stages"] * p["slot_bytes"] + (W - 1) * p["row_bytes"]
     assert W == 3 or (p["hb_width"] <= 1024 and p["vec"] == 4)
     assert p["ws_bytes"] == 0
 
