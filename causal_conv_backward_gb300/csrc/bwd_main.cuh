@@ -156,7 +156,9 @@ __device__ __forceinline__ Vf<NP> load_weight(const MainParams &p, int k, int64_
     return unpack<DT, NP>(r);
 }
 
-template <int DT, int R, int NP, int W>
+// BS: gradX rows leave through the slot with bulk copies (4 KB rows over long
+// CTA ranges) instead of per-thread streaming stores.
+template <int DT, int R, int NP, int W, bool BS = false>
 __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t r1, int ct, int lane)
 {
     const int NS = p.stages;
@@ -250,7 +252,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
         if (!dead && active) {
             const uint8_t *sl = smem + (size_t)slot * p.slot_bytes + 2 * CH * ct;
             const uint8_t *gys = sl;                                   // gradY slot rows 0..R+W-2
-            const uint8_t *xs = sl + (size_t)(R + WH) * p.row_bytes;   // x slot rows 0..R-1
+            uint8_t *xs = const_cast<uint8_t *>(sl) + (size_t)(R + WH) * p.row_bytes;   // x slot rows 0..R-1
             const uint8_t *ms = smem + p.off_mask + 32u * slot;
             if (head) {
 #pragma unroll
@@ -287,7 +289,16 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                     for (int k = 0; k < W; ++k)
                         acc[W - 1 - k][e] = fma2(k < WH ? win[k].e[e] : gn.e[e], xv.e[e], acc[W - 1 - k][e]);
                 }
-                store_cs<NP>(gxp + (int64_t)r * row_stride, o);
+                if constexpr (BS) {
+                    // x(i+r) was read from this slot row above and is dead
+                    // now: the row takes gradX(i+r) instead
+                    if constexpr (NP == 4)
+                        *reinterpret_cast<uint4 *>(xs + (size_t)r * p.row_bytes) = make_uint4(o[0], o[1], o[2], o[3]);
+                    else
+                        *reinterpret_cast<uint2 *>(xs + (size_t)r * p.row_bytes) = make_uint2(o[0], o[1]);
+                } else {
+                    store_cs<NP>(gxp + (int64_t)r * row_stride, o);
+                }
 #pragma unroll
                 for (int q = 0; q + 1 < WH; ++q)
                     win[q] = win[q + 1];
@@ -325,9 +336,29 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                 since_flush = 0;
             }
         }
-        __syncwarp();
-        if (!dead && lane == 0)
-            mbar_arrive(bar_empty0 + 8u * slot);
+        if constexpr (BS) {
+            // every consumer's gradX values of the stage are in the slot
+            // (made visible to the bulk-copy engine); one thread stores the
+            // rows and releases the slot once the copies have read it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"r"(nct) : "memory");
+            if (ct == 0 && !dead) {
+                const int64_t hb0 = (int64_t)cur.hb * p.hb_width;
+                const int64_t width = (p.H - hb0 < p.hb_width) ? (p.H - hb0) : p.hb_width;
+                const uint32_t xbase =
+                    smem_u32(smem + (size_t)slot * p.slot_bytes) + (uint32_t)(R + WH) * p.row_bytes;
+                for (int r = 0; r < n; ++r)
+                    bulk_s2g(p.gx + 2 * (((cur.i + r) * p.B + cur.j) * p.H + hb0), xbase + (uint32_t)r * p.row_bytes,
+                             (uint32_t)width * 2u);
+                bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(bar_empty0 + 8u * slot);
+            }
+        } else {
+            __syncwarp();
+            if (!dead && lane == 0)
+                mbar_arrive(bar_empty0 + 8u * slot);
+        }
         cur.advance(n, p.S, p.B);
         ++stage;
         if (++slot == NS) {
@@ -337,11 +368,13 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     }
     if (hb_cur >= 0)
         flush_partial();
+    if (BS && ct == 0)
+        bulk_wait_all();   // the gradX rows are written
     return dead;
 }
 
 // ------------------------------------------------------------------ kernels
-template <int DT, int R, int NP, int W>
+template <int DT, int R, int NP, int W, bool BS>
 __device__ __forceinline__ void main_body(const MainParams &p)
 {
     // one producer lane per staged row (R + W - 1 gradY rows, R x rows), and
@@ -358,7 +391,7 @@ __device__ __forceinline__ void main_body(const MainParams &p)
         const uint32_t bar0 = smem_u32(smem + p.off_bar);
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(bar0 + 8u * s, 1);                                    // full
-            mbar_init(bar0 + 8u * (p.stages + s), (uint32_t)consumer_warps);  // empty
+            mbar_init(bar0 + 8u * (p.stages + s), BS ? 1u : (uint32_t)consumer_warps);  // empty
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -375,7 +408,7 @@ __device__ __forceinline__ void main_body(const MainParams &p)
     if (threadIdx.x < 32)
         dead = produce<R, W>(p, smem, r0, r1, lane);
     else
-        dead = consume<DT, R, NP, W>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
+        dead = consume<DT, R, NP, W, BS>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
     if (dead && lane == 0)
         atomicOr(&s_err, 1);
     __syncthreads();
@@ -389,10 +422,10 @@ __device__ __forceinline__ void main_body(const MainParams &p)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <int DT, int R, int NP, int W>
+template <int DT, int R, int NP, int W, bool BS = false>
 __global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_constant__ MainParams p)
 {
-    main_body<DT, R, NP, W>(p);
+    main_body<DT, R, NP, W, BS>(p);
 }
 
 // The same kernel held to the registers that let two CTAs share an SM
@@ -400,7 +433,7 @@ __global__ void __launch_bounds__(kMaxThreads) mcc1d_bwd_main(const __grid_const
 template <int DT, int R, int NP, int W>
 __global__ void __launch_bounds__(kMaxThreads, 2) mcc1d_bwd_main_x2(const __grid_constant__ MainParams p)
 {
-    main_body<DT, R, NP, W>(p);
+    main_body<DT, R, NP, W, false>(p);
 }
 
 typedef void (*MainFn)(MainParams);

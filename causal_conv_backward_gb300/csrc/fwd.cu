@@ -61,13 +61,6 @@ struct FwdParams {
     int32_t w_vec;         // weight rows can be read as aligned vectors
 };
 
-// Shared -> global bulk copy of one row, in the thread's bulk-async group.
-__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
-
 // Byte q of a stage (row cursor at output row t = c.i): q < W-1 says whether
 // the halo row t-(W-1)+q exists (is >= 0); q >= W-1 is the output mask of row
 // t+q-(W-1) (zero past the end of S).
@@ -287,8 +280,8 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                 for (int r = 0; r < n; ++r)
                     bulk_s2g(p.y + 2 * (((cur.i + r) * p.B + cur.j) * p.H + hb0), sbase + (uint32_t)r * p.row_bytes,
                              (uint32_t)width * 2u);
-                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                bulk_commit();
+                bulk_wait_read_all();
                 mbar_arrive(bar_empty0 + 8u * slot);
             }
         } else {
@@ -304,7 +297,7 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
         }
     }
     if (BS && ct == 0)
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the y rows are written
+        bulk_wait_all();   // the y rows are written
     return dead;
 }
 

@@ -152,8 +152,20 @@ __global__ void __launch_bounds__(256) mcc1d_pack(const uint16_t *src, int64_t s
 typedef void (*ReduceFn)(ReduceParams);
 
 template <int DT, int NP>
-static MainFn main_for(int R)
+static MainFn main_for(int R, bool bulk)
 {
+    if (bulk) {
+        // bulk gradX stores: 4 KB rows only, which take 8 channels per thread
+        if constexpr (NP == 4) {
+            switch (R) {
+            case 4: return mcc1d_bwd_main<DT, 4, NP, 3, true>;
+            case 6: return mcc1d_bwd_main<DT, 6, NP, 3, true>;
+            case 8: return mcc1d_bwd_main<DT, 8, NP, 3, true>;
+            default: return nullptr;
+            }
+        }
+        return nullptr;
+    }
     switch (R) {
     case 4: return mcc1d_bwd_main<DT, 4, NP, 3>;
     case 6: return mcc1d_bwd_main<DT, 6, NP, 3>;
@@ -170,13 +182,21 @@ static MainFn main_for(int R)
 // Instances for W != 3 (R = 6) live in kernels_w.cu.
 MainFn main_kernel_other_w(int dtype, int vec, int W);
 
-static MainFn main_kernel(int dtype, int R, int vec, int W)
+static MainFn main_kernel(int dtype, int R, int vec, int W, bool bulk)
 {
     if (W != 3)
-        return R == 6 ? main_kernel_other_w(dtype, vec, W) : nullptr;
+        return R == 6 && !bulk ? main_kernel_other_w(dtype, vec, W) : nullptr;
     if (dtype == 0)
-        return vec == 4 ? main_for<0, 2>(R) : main_for<0, 4>(R);
-    return vec == 4 ? main_for<1, 2>(R) : main_for<1, 4>(R);
+        return vec == 4 ? main_for<0, 2>(R, bulk) : main_for<0, 4>(R, bulk);
+    return vec == 4 ? main_for<1, 2>(R, bulk) : main_for<1, 4>(R, bulk);
+}
+
+// gradX leaves by bulk copies out of the ring on 4 KB rows (8 channels per
+// thread, W = 3) over long CTA ranges: +1.3 % on the 512K-token workload;
+// narrow rows and short ranges lose to the per-stage barrier and wait.
+static bool bwd_bulk_store(const Plan &pl)
+{
+    return pl.W == 3 && pl.vec == 8 && pl.row_bytes >= 4096 && pl.rows_total / pl.ncta >= kWideMinRowsPerCta;
 }
 
 // cudaFuncSetAttribute once per (kernel, device, context): a context created
@@ -314,7 +334,7 @@ int32_t launch_bwd(const Plan &pl, const Layout &L, const void *gradY, const voi
     mp.w_vec = (L.w[1] == 1 && (L.w[0] * 2) % 16 == 0 && ((uintptr_t)weight & 15u) == 0) ? 1 : 0;
 
     const int R = pl.rows_per_stage;
-    MainFn mfn = main_kernel(pl.dtype, R, pl.vec, pl.W);
+    MainFn mfn = main_kernel(pl.dtype, R, pl.vec, pl.W, bwd_bulk_store(pl));
     if (!mfn)
         return kErrCuda;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(mfn)))

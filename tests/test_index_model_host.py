@@ -71,6 +71,7 @@ def model_backward(S, B, H, W, kind, full):
     rb, sb = p["row_bytes"], p["slot_bytes"]
     cw = p["consumer_warps"]
     contig = B == 1 and p["n_hb"] == 1 and p["rows_total"] // p["ncta"] < KDEEP
+    bulk = W == 3 and vec == 8 and rb >= 4096 and p["rows_total"] // p["ncta"] >= 1024
     written = np.zeros(E // vec, np.int32) if full else None
     part_elems = p["nslots"] * W * hbw
     used_slots = set()
@@ -95,6 +96,11 @@ def model_backward(S, B, H, W, kind, full):
                     check_copy((i + q) * B * H + j * H + hb0, wbytes, E, q * rb, gy_rows_end)
                 for q in range(n):
                     check_copy((i + q) * B * H + j * H + hb0, wbytes, E, gy_rows_end + q * rb, sb)
+            if bulk:
+                # gradX rows leave from the x slot rows, one bulk copy
+                # (shared -> global) per row
+                for r in range(n):
+                    check_copy((i + r) * B * H + j * H + hb0, wbytes, E, gy_rows_end + r * rb, sb)
             # consumer stores of gradX: rows i .. i+n-1, active threads only
             ct = np.arange(cw * 32)
             ct = ct[vec * ct < width]
