@@ -122,3 +122,17 @@ def test_forward_width_full_size(W):
     y = run_fwd(inp, wl.S, wl.B, wl.H, wl.dtype, W=W)
     ref = oracle.fwd_bits(wl.S, wl.B, wl.H, W, wl.dtype, inp["x"], inp["w"], inp["mask"])
     assert max_ulp(y, ref) <= GX_MAX_ULP
+
+
+# 4 KB rows over CTA ranges of at least 1024 rows: y leaves by bulk copies.
+BULK = [(20000, 8, 4096, "bf16", ("spans", 0.2, 64, 1024)), (12000, 16, 6144, "fp16", ("bernoulli", 0.9)),
+        (40001, 4, 4096, "fp16", ("prefix",))]
+
+
+@pytest.mark.parametrize("S,B,H,dt,mask", BULK, ids=[f"s{a}_b{b}_h{c}_{d}_{e[0]}" for a, b, c, d, e in BULK])
+def test_forward_bulk_store_plans(S, B, H, dt, mask):
+    wl = datagen.Workload("fbulk", S, B, H, dt, mask=mask)
+    inp = datagen.generate(wl, seed=S + 7)
+    y = run_fwd(inp, S, B, H, dt)
+    ref = oracle.fwd_bits(S, B, H, 3, dt, inp["x"], inp["w"], inp["mask"])
+    assert max_ulp(y, ref) <= GX_MAX_ULP

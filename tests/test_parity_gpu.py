@@ -234,3 +234,23 @@ def test_repeated_calls_match_oracle(S, B, H, dt):
         else:
             assert np.array_equal(gx, first[0]) and np.array_equal(gw, first[1]), it
         ws.fill_(0xFF if it % 2 else 0x3F)
+
+
+# ------------------------------------------------------------- bulk-store plans
+# 4 KB rows (2048-channel H-blocks) over CTA ranges of at least 1024 rows send
+# gradX (and the forward's y) out of the ring with bulk copies. These shapes
+# reach those plans with other masks, dtypes, H-block counts and sequence
+# ends than the full workloads.
+BULK = [(20000, 8, 4096, "bf16", ("spans", 0.2, 64, 1024)), (12000, 16, 6144, "fp16", ("bernoulli", 0.9)),
+        (40001, 4, 4096, "fp16", ("prefix",)), (10000, 16, 4096, "bf16", ("none",))]
+
+
+@pytest.mark.parametrize("S,B,H,dt,mask", BULK, ids=[f"s{a}_b{b}_h{c}_{d}_{e[0]}" for a, b, c, d, e in BULK])
+def test_bulk_store_plans(S, B, H, dt, mask):
+    import causal_conv_backward_gb300 as m
+    p = m.mcc1d_plan_describe(S, B, H, 3, dt, m.PLAN_BWD)
+    assert p["hb_width"] == 2048 and p["vec"] == 8 and p["rows_total"] // p["ncta"] >= 1024
+    wl = datagen.Workload("bulk", S, B, H, dt, mask=mask)
+    inp = datagen.generate(wl, seed=S + H)
+    gx, gw, status, _ = run_cuda(inp, S, B, H, dt)
+    check_against_oracle(wl, inp, gx, gw, status)

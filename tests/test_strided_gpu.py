@@ -133,3 +133,20 @@ def test_backward_helper_accepts_views():
     torch.cuda.synchronize()
     assert torch.equal(gx_s.view(torch.int16), gx_d.view(torch.int16))
     assert torch.equal(gw_s.view(torch.int16), gw_d.view(torch.int16))
+
+
+def test_strided_bulk_store_plan():
+    """[B,S,H] memory seen as [S,B,H] on a plan whose gradX leaves by bulk
+    copies (4 KB rows, long CTA ranges): the same bits as the dense call."""
+    S, B, H, dt = 16384, 8, 4096, "fp16"
+    p = m.mcc1d_plan_describe(S, B, H, 3, dt, m.PLAN_BWD_EX)
+    assert p["hb_width"] == 2048 and p["rows_total"] // p["ncta"] >= 1024
+    wl = datagen.Workload("sbulk", S, B, H, dt, mask=("bernoulli", 0.9))
+    inp = datagen.generate(wl, seed=77)
+    gy, x, w = (to_device(inp[k], dt) for k in ("gy", "x", "w"))
+    mask = torch.from_numpy(inp["mask"]).cuda()
+    gx_d, gw_d = run_dense(gy, x, w, mask, S, B, H, dt)
+    gx_s, gw_s, _ = run_ex(make_view(gy, "bsh"), make_view(x, "bsh"), w, mask, S, B, H, dt)
+    torch.cuda.synchronize()
+    assert torch.equal(gx_s.view(torch.int16), gx_d.view(torch.int16))
+    assert torch.equal(gw_s.view(torch.int16), gw_d.view(torch.int16))
