@@ -168,6 +168,14 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     constexpr int CH = 2 * NP;                                     // channels per thread
     constexpr int WH = W - 1;                                      // rows of the window
     constexpr bool kStageSums = W <= 3;                            // per-stage gradWeight level
+    // Wide kernels (cert_uses_plain_sum): gradX by a certified plain sum,
+    // the cascade only where the certificate fails (see below).
+    constexpr bool kCF = cert_uses_plain_sum(DT, W) && !BS;
+    constexpr float kCert = cert_factor<DT>();
+    // the fallback finds the W-1 rows before a stage in the previous slot,
+    // whose look-ahead holds R rows; one failure bit per (row, channel pair)
+    static_assert(!kCF || W - 1 <= R, "certified sums need W - 1 <= R");
+    static_assert(!kCF || R * NP <= 32, "one 32-bit failure mask per stage");
     float *outer = reinterpret_cast<float *>(smem + p.off_outer);  // [W*CH][nct]
     const int64_t row_stride = 2 * (int64_t)p.B * p.H;             // bytes from row i to i+1
     const int c = blockIdx.x;
@@ -228,6 +236,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     int slot = 0, stage = 0;
     uint32_t ph = 0;
     bool dead = false;
+    int prev_slot = -1, n_prev = 0;
     while (cur.pos < r1) {
         const int n = cur.rows<R>(p.S);
         const bool head = (stage == 0) || (cur.i == 0);
@@ -272,6 +281,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                 for (int e = 0; e < NP; ++e)
                     in[k][e] = make_float2(0.f, 0.f);
             float2 (&acc)[W][NP] = kStageSums ? in : mid;
+            uint32_t fails = 0;
             // One row i+r: gradX from the window gYm(i+r .. i+r+W-2) and the
             // staged gradY row i+r+W-1; the W gradWeight taps against x(i+r).
             auto row = [&](int r) {
@@ -282,8 +292,27 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                 for (int e = 0; e < NP; ++e) {
                     // gradX = sum_k gYm(i+k) w(W-1-k): exact fp32 products,
                     // a compensated sum, rounded once (sum_to16)
-                    o[e] = sum_to16<DT, W>(
-                        [&](int k) { return mul2(k < WH ? win[k].e[e] : gn.e[e], wt[W - 1 - k].e[e]); });
+                    if constexpr (kCF) {
+                        // plain pairwise sum s of the exact products and the
+                        // sum a of their magnitudes in the same tree; when
+                        // kCert * a <= |s|, round(s) is within 1 ulp of the
+                        // exact sum rounded once (cert_factor); else the
+                        // channel is recomputed after the stage
+                        float2 pk[W], ak[W];
+#pragma unroll
+                        for (int k = 0; k < W; ++k) {
+                            pk[k] = mul2(k < WH ? win[k].e[e] : gn.e[e], wt[W - 1 - k].e[e]);
+                            ak[k] = abs2(pk[k]);
+                        }
+                        const float2 sf = tree_sum<0, W, W>(pk);
+                        const float2 af = tree_sum<0, W, W>(ak);
+                        const bool ok = (kCert * af.x <= fabsf(sf.x)) & (kCert * af.y <= fabsf(sf.y));
+                        o[e] = pack2<DT>(sf);
+                        fails |= (ok ? 0u : 1u) << (r * NP + e);
+                    } else {
+                        o[e] = sum_to16<DT, W>(
+                            [&](int k) { return mul2(k < WH ? win[k].e[e] : gn.e[e], wt[W - 1 - k].e[e]); });
+                    }
                     // gradWeight tap k pairs x(i) with gYm(i+W-1-k)
 #pragma unroll
                     for (int k = 0; k < W; ++k)
@@ -316,6 +345,36 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                 for (int r = 0; r < R; ++r)
                     if (r < n)
                         row(r);
+            }
+            if constexpr (kCF) {
+                // channels whose certificate failed (a small fraction: strong
+                // cancellation): the cascade, from the staged rows; the rows
+                // before this stage are still in the previous slot, which is
+                // released one stage late for this
+                if (fails) {
+                    const uint8_t *psl = smem + (size_t)(prev_slot < 0 ? 0 : prev_slot) * p.slot_bytes + 2 * CH * ct;
+                    const uint8_t *pms = smem + p.off_mask + 32u * (prev_slot < 0 ? 0 : prev_slot);
+#pragma unroll 1
+                    for (int r = 0; r < n; ++r) {
+#pragma unroll
+                        for (int e = 0; e < NP; ++e) {
+                            if ((fails >> (r * NP + e)) & 1u) {
+                                float2 qk[W];
+#pragma unroll
+                                for (int k = 0; k < W; ++k) {
+                                    const int q = r + k;
+                                    const bool here = head || q >= WH;
+                                    const uint8_t *rp = here ? gys + (size_t)q * p.row_bytes
+                                                             : psl + (size_t)(n_prev + q) * p.row_bytes;
+                                    const uint8_t mb = here ? ms[q] : pms[n_prev + q];
+                                    qk[k] = mul2(load_masked<DT, NP>(rp, mb).e[e], wt[W - 1 - k].e[e]);
+                                }
+                                const uint32_t v = sum_to16<DT, W>([&](int k) { return qk[k]; });
+                                *reinterpret_cast<uint32_t *>(gxp + (int64_t)r * row_stride + 4 * e) = v;
+                            }
+                        }
+                    }
+                }
             }
             if constexpr (kStageSums) {
 #pragma unroll
@@ -354,6 +413,13 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                 bulk_wait_read_all();
                 mbar_arrive(bar_empty0 + 8u * slot);
             }
+        } else if constexpr (kCF) {
+            // the previous slot stays readable until this stage's fallback is done
+            __syncwarp();
+            if (!dead && lane == 0 && prev_slot >= 0)
+                mbar_arrive(bar_empty0 + 8u * prev_slot);
+            prev_slot = slot;
+            n_prev = n;
         } else {
             __syncwarp();
             if (!dead && lane == 0)
@@ -368,6 +434,11 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     }
     if (hb_cur >= 0)
         flush_partial();
+    if constexpr (kCF) {
+        __syncwarp();
+        if (!dead && lane == 0 && prev_slot >= 0)
+            mbar_arrive(bar_empty0 + 8u * prev_slot);
+    }
     if (BS && ct == 0)
         bulk_wait_all();   // the gradX rows are written
     return dead;

@@ -259,6 +259,54 @@ __device__ __forceinline__ uint32_t sum_to16(Prod prod)
         return pack2<DT>(s);
 }
 
+// |v| of both lanes (clears the sign bits).
+__device__ __forceinline__ float2 abs2(float2 v)
+{
+    return make_float2(__uint_as_float(__float_as_uint(v.x) & 0x7FFFFFFFu),
+                       __uint_as_float(__float_as_uint(v.y) & 0x7FFFFFFFu));
+}
+
+// Pairwise sum of v[LO .. LO+N) in a fixed tree: the first half is the
+// largest power of two below N, so no element passes more than ceil(log2 N)
+// additions.
+template <int LO, int N, int W>
+__device__ __forceinline__ float2 tree_sum(const float2 (&v)[W])
+{
+    if constexpr (N == 1) {
+        return v[LO];
+    } else {
+        constexpr int kHalf = N > 4 ? 4 : (N > 2 ? 2 : 1);
+        return add2(tree_sum<LO, kHalf, W>(v), tree_sum<LO + kHalf, N - kHalf, W>(v));
+    }
+}
+
+// Certificate for a pairwise sum s of W <= 8 exact products (tree depth 3)
+// whose magnitudes sum to a (same tree): |s - exact| <= gamma_3 * sum|p| <=
+// 3u(1 + 4u) a (Higham, "Accuracy and Stability of Numerical Algorithms",
+// 2nd ed., section 4.2; u = 2^-24). The 16-bit grid's spacing at x exceeds
+// x * 2^-(m+1) (m + 1 significant bits: 11 for fp16, 8 for bf16), so if
+// that error bound is below (|s| - bound) * 2^-(m+1), s and the exact sum lie
+// closer than the smallest spacing between them: at most one rounding
+// boundary separates them and round(s) is within 1 ulp of the exact sum
+// rounded once. The test kCert * a <= |s| implies this, with slack for the
+// roundings of a and of the product.
+constexpr int kCertMinW = 6;
+// Where the certified sum replaces the cascade: bf16 from W = 6 (below that
+// the kernels are not bound by their sums); fp16 at W = 8 only. fp16 has 10
+// fraction bits to bf16's 7, so its certificate is 8x tighter and fails about
+// 8x as often on the same data; a warp with one failing lane pays the whole
+// recompute, and at W = 6, 7 the cascade measured faster.
+__host__ __device__ constexpr bool cert_uses_plain_sum(int DT, int W)
+{
+    return W >= kCertMinW && (DT == 0 || W == 8);
+}
+template <int DT>
+__host__ __device__ constexpr float cert_factor()
+{
+    // 3 * 2^-24 * 2^(m+1) / (1 - 2^-m) * (1 + 2^-20), rounded up
+    return DT == 1 ? 3.f * 1.220703125e-4f * 1.0011f : 3.f * 1.52587890625e-5f * 1.0081f;
+}
+
 // ------------------------------------------------------------------ row cursor
 // Position in the flattened (hb, j, i) row sequence of one CTA range.
 struct Cursor {

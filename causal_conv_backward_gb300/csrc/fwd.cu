@@ -179,6 +179,15 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
 {
     constexpr int CH = 2 * NP;
     constexpr int WH = W - 1;                  // rows of the window
+    // Wide kernels: y by the backward's certified plain sum, the cascade
+    // only for channels whose certificate fails, recomputed after the stage
+    // from the staged rows (the slot keeps x rows: not with bulk stores).
+    constexpr bool kCF = cert_uses_plain_sum(DT, W) && !BS;
+    constexpr float kCert = cert_factor<DT>();
+    // the W-1 rows before a stage that follows a full stage are the previous
+    // slot's last rows; one failure bit per (row, channel pair)
+    static_assert(!kCF || W - 1 <= R, "certified sums need W - 1 <= R");
+    static_assert(!kCF || R * NP <= 32, "one 32-bit failure mask per stage");
     const int NS = p.stages;
     const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
@@ -197,6 +206,7 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
     int slot = 0, stage = 0;
     uint32_t ph = 0;
     bool dead = false;
+    int prev_slot = -1, n_prev = 0;
     while (cur.pos < r1) {
         const int n = cur.rows<R>(p.S);
         const bool head = (stage == 0) || (cur.i == 0);
@@ -228,17 +238,35 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                     win[q] = load_masked<DT, NP>(hs + (size_t)q * p.row_bytes, ms[q]);
             }
             uint8_t *yp = p.y + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
+            uint32_t fails = 0;
             auto row = [&](int r) {
                 const Vf<NP> xn = unpack<DT, NP>(load_raw<NP>(xs + (size_t)r * p.row_bytes));
                 const uint32_t keep = 0u - (uint32_t)ms[r + WH];
                 uint32_t o[NP];
 #pragma unroll
                 for (int e = 0; e < NP; ++e) {
-                    // exact fp32 products, summed and rounded once by
-                    // sum_to16 (the backward's gradX sum)
-                    o[e] = sum_to16<DT, W>(
-                               [&](int k) { return mul2(k < WH ? win[k].e[e] : xn.e[e], wt[k].e[e]); }) &
-                           keep;  // output mask
+                    if constexpr (kCF) {
+                        // plain pairwise sums of the exact products and of
+                        // their magnitudes; kept when kCert * a <= |s|
+                        // (within 1 ulp of the exact sum rounded once)
+                        float2 pk[W], ak[W];
+#pragma unroll
+                        for (int k = 0; k < W; ++k) {
+                            pk[k] = mul2(k < WH ? win[k].e[e] : xn.e[e], wt[k].e[e]);
+                            ak[k] = abs2(pk[k]);
+                        }
+                        const float2 sf = tree_sum<0, W, W>(pk);
+                        const float2 af = tree_sum<0, W, W>(ak);
+                        const bool ok = (kCert * af.x <= fabsf(sf.x)) & (kCert * af.y <= fabsf(sf.y));
+                        o[e] = pack2<DT>(sf) & keep;
+                        fails |= (ok ? 0u : 1u) << (r * NP + e);
+                    } else {
+                        // exact fp32 products, summed and rounded once by
+                        // sum_to16 (the backward's gradX sum)
+                        o[e] = sum_to16<DT, W>(
+                                   [&](int k) { return mul2(k < WH ? win[k].e[e] : xn.e[e], wt[k].e[e]); }) &
+                               keep;  // output mask
+                    }
                 }
                 if constexpr (BS) {
                     // x(t+r) was read from this slot row above and now lives
@@ -266,6 +294,40 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                     if (r < n)
                         row(r);
             }
+            if constexpr (kCF) {
+                // failed channels (strong cancellation): the cascade over
+                // x(t+r-W+1) .. x(t+r), from this slot, the halo area at a
+                // head stage, else the previous slot (released one stage
+                // late for this); the stored value is overwritten
+                if (fails) {
+                    const uint8_t *hs = smem + p.off_halo + 2 * CH * ct;
+                    const uint8_t *psl = smem + (size_t)(prev_slot < 0 ? 0 : prev_slot) * p.slot_bytes + 2 * CH * ct;
+#pragma unroll 1
+                    for (int r = 0; r < n; ++r) {
+                        const uint32_t keep = 0u - (uint32_t)ms[r + WH];
+#pragma unroll
+                        for (int e = 0; e < NP; ++e) {
+                            if ((fails >> (r * NP + e)) & 1u) {
+                                float2 qk[W];
+#pragma unroll
+                                for (int k = 0; k < W; ++k) {
+                                    const int d = r + k - WH;   // x row relative to the stage's first
+                                    Vf<NP> xv;
+                                    if (d >= 0)
+                                        xv = unpack<DT, NP>(load_raw<NP>(xs + (size_t)d * p.row_bytes));
+                                    else if (head)
+                                        xv = load_masked<DT, NP>(hs + (size_t)(WH + d) * p.row_bytes, ms[WH + d]);
+                                    else
+                                        xv = unpack<DT, NP>(load_raw<NP>(psl + (size_t)(n_prev + d) * p.row_bytes));
+                                    qk[k] = mul2(xv.e[e], wt[k].e[e]);
+                                }
+                                const uint32_t v = sum_to16<DT, W>([&](int k) { return qk[k]; }) & keep;
+                                *reinterpret_cast<uint32_t *>(yp + (int64_t)r * row_stride + 4 * e) = v;
+                            }
+                        }
+                    }
+                }
+            }
         }
         if constexpr (BS) {
             // every consumer's y values of the stage are in the slot (their
@@ -284,6 +346,13 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                 bulk_wait_read_all();
                 mbar_arrive(bar_empty0 + 8u * slot);
             }
+        } else if constexpr (kCF) {
+            // the previous slot stays readable until this stage's fallback is done
+            __syncwarp();
+            if (!dead && lane == 0 && prev_slot >= 0)
+                mbar_arrive(bar_empty0 + 8u * prev_slot);
+            prev_slot = slot;
+            n_prev = n;
         } else {
             __syncwarp();
             if (!dead && lane == 0)
@@ -295,6 +364,11 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             slot = 0;
             ph ^= 1u;
         }
+    }
+    if constexpr (kCF) {
+        __syncwarp();
+        if (!dead && lane == 0 && prev_slot >= 0)
+            mbar_arrive(bar_empty0 + 8u * prev_slot);
     }
     if (BS && ct == 0)
         bulk_wait_all();   // the y rows are written

@@ -179,13 +179,13 @@ static MainFn main_for(int R, bool bulk)
     }
 }
 
-// Instances for W != 3 (R = 6) live in kernels_w.cu.
-MainFn main_kernel_other_w(int dtype, int vec, int W);
+// Instances for W != 3 live in kernels_w.cu.
+MainFn main_kernel_other_w(int dtype, int vec, int W, int R);
 
 static MainFn main_kernel(int dtype, int R, int vec, int W, bool bulk)
 {
     if (W != 3)
-        return R == 6 && !bulk ? main_kernel_other_w(dtype, vec, W) : nullptr;
+        return bulk ? nullptr : main_kernel_other_w(dtype, vec, W, R);
     if (dtype == 0)
         return vec == 4 ? main_for<0, 2>(R, bulk) : main_for<0, 4>(R, bulk);
     return vec == 4 ? main_for<1, 2>(R, bulk) : main_for<1, 4>(R, bulk);

@@ -1,0 +1,138 @@
+"""The certificate of the backward's plain gradX sum at widths 6..8.
+
+At W >= 6 the backward's main kernel sums the W exact fp32 products of a
+gradX value in a fixed pairwise tree and keeps the result when
+cert_factor * (the same tree over |products|) <= |sum|; otherwise the channel
+is recomputed with the compensated cascade. The claim is that every kept
+value, rounded once to the 16-bit type, is within 1 ulp of the exact sum
+rounded once (the acceptance bar of the page's gradX).
+
+These CPU tests check the claim by simulation, independently of the kernel's
+build: the factors in device_common.cuh are read as text and compared with
+the bound they rest on, and the fp32 tree (IEEE round-to-nearest additions,
+as add.rn.f32x2 does) runs in numpy on seeded inputs built for heavy
+cancellation, where the certificate is tight. Exact sums come from float64,
+exact here because the inputs span a narrow exponent range.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "causal_conv_backward_gb300", "csrc", "device_common.cuh")
+
+# significand bits after the point: fp16 10, bf16 7 (dtype codes: bf16 0, fp16 1)
+MBITS = {"fp16": 10, "bf16": 7}
+
+
+def header_factors():
+    """(fp16 factor, bf16 factor) as written in cert_factor<DT>()."""
+    txt = open(HEADER).read()
+    body = txt[txt.index("constexpr float cert_factor()"):]
+    body = body[:body.index("}")]
+    m = re.search(r"DT == 1 \? ([^:]+) : ([^;]+);", body)
+    assert m, "cert_factor's expression not found"
+
+    def ev(expr):
+        terms = [t.strip().rstrip("f") for t in expr.split("*")]
+        v = 1.0
+        for t in terms:
+            v *= float(t)
+        return v
+
+    return ev(m.group(1)), ev(m.group(2))
+
+
+def needed_factor(mbits):
+    """Smallest factor the argument accepts: gamma_3 (three roundings of
+    u = 2^-24 on any path of a depth-3 tree) against half the 16-bit
+    relative spacing 2^-(m+1), with the distance |s| - bound, and a little for
+    the roundings of the magnitude sum and of the factor's product."""
+    u = 2.0 ** -24
+    gamma3 = 3 * u / (1 - 3 * u)
+    return gamma3 * 2.0 ** (mbits + 1) / (1 - 2.0 ** -mbits) * (1 + 2.0 ** -20)
+
+
+def test_header_factors_cover_the_bound():
+    f16, b16 = header_factors()
+    assert np.float32(f16) >= needed_factor(MBITS["fp16"])
+    assert np.float32(b16) >= needed_factor(MBITS["bf16"])
+    # and not loose by more than 0.2 %, which would only cost fallbacks
+    assert f16 <= 1.002 * needed_factor(MBITS["fp16"])
+    assert b16 <= 1.002 * needed_factor(MBITS["bf16"])
+
+
+def to_bf16(a):
+    """float32 -> nearest bf16 (ties to even), as float32 values."""
+    b = np.asarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16 << 16
+    return b.astype(np.uint32).view(np.float32)
+
+
+def round16(x, dt):
+    """Exact float64 x -> nearest 16-bit value (ties to even), normal range."""
+    if dt == "fp16":
+        return x.astype(np.float16).astype(np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 2.0 ** 8), e - 8)
+
+
+def ulp16(x, dt):
+    m, e = np.frexp(np.abs(x))
+    return np.ldexp(np.ones_like(x), e - 1 - MBITS[dt])
+
+
+def tree(v):
+    """The kernel's pairwise tree over v[..., 0:W] in float32: halves of 4,
+    2, 1 (W = 6: (01 + 23) + 45; 7: (01 + 23) + (45 + 6); 8: (01 + 23) + (45 + 67))."""
+    def rec(lo, n):
+        if n == 1:
+            return v[:, lo]
+        half = 4 if n > 4 else (2 if n > 2 else 1)
+        return (rec(lo, half) + rec(lo + half, n - half)).astype(np.float32)
+    return rec(0, v.shape[1])
+
+
+def operands(rng, n, W, dt, cancel):
+    """n rows of W gradY and weight values in the 16-bit type, exponents in
+    [-4, 4]; with `cancel`, the last product is set close to minus the sum
+    of the others (the cancellation that makes the certificate fail)."""
+    conv = (lambda a: a.astype(np.float16).astype(np.float32)) if dt == "fp16" else to_bf16
+    g = conv(rng.uniform(1, 2, (n, W)) * 2.0 ** rng.integers(-4, 4, (n, W)) * rng.choice([-1, 1], (n, W)))
+    w = conv(rng.uniform(1, 2, (n, W)) * 2.0 ** rng.integers(-4, 4, (n, W)) * rng.choice([-1, 1], (n, W)))
+    if cancel:
+        rest = (g[:, :-1].astype(np.float64) * w[:, :-1]).sum(1)
+        target = -rest * (1 + rng.normal(0, 2.0 ** -rng.integers(4, 20, n)))
+        w[:, -1] = conv(np.clip(np.abs(target / g[:, -1]), 2.0 ** -4, 2.0 ** 5)
+                        * np.sign(target / g[:, -1]))
+    return g, w
+
+
+@pytest.mark.parametrize("dt", ["fp16", "bf16"])
+@pytest.mark.parametrize("W", [6, 7, 8])
+def test_every_certified_sum_is_within_one_ulp(dt, W):
+    f16, b16 = header_factors()
+    cert = np.float32(f16 if dt == "fp16" else b16)
+    rng = np.random.default_rng(1000 * W + (dt == "fp16"))
+    kept = failed = 0
+    for cancel in (False, True):
+        g, w = operands(rng, 60000, W, dt, cancel)
+        p32 = g * w                                          # exact in fp32
+        p64 = g.astype(np.float64) * w.astype(np.float64)
+        assert np.array_equal(p32.astype(np.float64), p64)
+        s = tree(p32)
+        a = tree(np.abs(p32))
+        ok = (cert * a).astype(np.float32) <= np.abs(s)
+        exact = p64.sum(1)                                   # exact: narrow exponent range
+        nz = exact != 0
+        ok &= nz
+        got = round16(s[ok].astype(np.float64), dt)
+        ref = round16(exact[ok], dt)
+        err = np.abs(got - ref) / ulp16(ref, dt)
+        assert err.max(initial=0) <= 1.0, (dt, W, cancel, err.max())
+        kept += int(ok.sum())
+        failed += int((~ok & nz).sum())
+    # the simulation exercises both outcomes
+    assert kept > 60000 and failed > 1000, (kept, failed)

@@ -7,7 +7,10 @@ B = 1 ranges) and checks, with no GPU: every bulk copy reads inside its
 tensor, starts on a 16-byte boundary, moves a multiple of 16 bytes and lands
 inside its ring slot; no stage needs more producer lanes than a warp has;
 every output element is written exactly once; every partial-sum write stays
-inside its slot. A kernel that broke one of these would fault or corrupt
+inside its slot. From W = 6 the kernels recompute, after a stage, the sums
+whose certificate failed from the rows still in shared memory: every such
+read must find the row it wants (in this slot, the halo area, or the
+previous slot, which the consumers release one stage late). A kernel that broke one of these would fault or corrupt
 memory on the GPU; here the mistake fails on the CPU first.
 """
 import numpy as np
@@ -75,8 +78,12 @@ def model_backward(S, B, H, W, kind, full):
     written = np.zeros(E // vec, np.int32) if full else None
     part_elems = p["nslots"] * W * hbw
     used_slots = set()
+    cert = W >= 6 and not bulk
+    if cert:
+        assert p["stages"] >= 2      # the previous slot is held while this one is read
     for c in ctas_to_check(p["ncta"], full):
         segs = set()
+        prev = None
         for stage, i, j, hb, n in walk(p, c):
             head = stage == 0 or i == 0
             hb0 = hb * hbw
@@ -84,6 +91,20 @@ def model_backward(S, B, H, W, kind, full):
             wbytes = 2 * width
             q0 = 0 if head else W - 1
             q1 = min(n + W - 1, S - i)
+            if cert:
+                # the fallback for row r reads gradY row i+q, q = r .. r+W-1:
+                # slot row q when staged here, else the previous slot's row
+                # n_prev + q (same sequence, staged there)
+                for r in range(n):
+                    for q in range(r, r + W):
+                        if i + q >= S:
+                            continue            # past the sequence: mask byte 0
+                        if head or q >= W - 1:
+                            assert q0 <= q < q1
+                        else:
+                            pi, pj, phb, pn, pq0, pq1 = prev
+                            assert (pj, phb) == (j, hb) and pi + pn == i
+                            assert pq0 <= pn + q < pq1
             nG = max(0, q1 - q0)
             gy_rows_end = (R + W - 1) * rb          # gradY rows 0 .. R+W-2, then x rows
             if contig:
@@ -110,6 +131,7 @@ def model_backward(S, B, H, W, kind, full):
                 if written is not None:
                     np.add.at(written, e // vec, 1)
             segs.add(hb)
+            prev = (i, j, hb, n, q0, q1)
         for hb in segs:
             slot = p["slot_base"][hb] + c - p["c_lo"][hb]
             assert 0 <= slot < p["nslots"] and slot not in used_slots
@@ -131,7 +153,11 @@ def model_forward(S, B, H, W, full):
     written = np.zeros(E // vec, np.int32) if full else None
     halo = (W - 1) * rb
     bulk = W == 3 and vec == 8 and rb >= 4096 and p["rows_total"] // p["ncta"] >= 1024
+    cert = W >= 6 and not bulk
+    if cert:
+        assert p["stages"] >= 2
     for c in ctas_to_check(p["ncta"], full):
+        prev = None
         for stage, i, j, hb, n in walk(p, c):
             hb0 = hb * hbw
             width = min(hbw, H - hb0)
@@ -144,6 +170,22 @@ def model_forward(S, B, H, W, full):
                 h0 = 0 if i >= W - 1 else W - 1 - i
             nh = W - 1 - h0
             assert n + nh <= 32
+            if cert:
+                # the fallback for row r reads x row i+d, d = r-W+1 .. r:
+                # slot row d; before the stage, the halo row W-1+d at a head
+                # stage (staged, or zero before the sequence start), else
+                # the previous slot's row n_prev + d
+                head = stage == 0 or i == 0
+                for r in range(n):
+                    for d in range(r - W + 1, r + 1):
+                        if d >= 0:
+                            assert d < n
+                        elif head:
+                            assert W - 1 + d >= h0 or i + d < 0
+                        else:
+                            pi, pj, phb, pn = prev
+                            assert (pj, phb) == (j, hb) and pi + pn == i
+                            assert 0 <= pn + d < pn
             if contig:
                 check_copy(i * H, n * wbytes, E, 0, sb)
                 if nh:
@@ -165,6 +207,7 @@ def model_forward(S, B, H, W, full):
                 assert e.max() + vec <= E
                 if written is not None:
                     np.add.at(written, e // vec, 1)
+            prev = (i, j, hb, n)
     if written is not None:
         assert written.min() == 1 and written.max() == 1
 
@@ -185,7 +228,7 @@ def test_backward_model_large_sampled_ctas(S, B, H):
     model_backward(S, B, H, 3, m.PLAN_BWD, full=False)
 
 
-@pytest.mark.parametrize("W", [1, 2, 4, 5, 8])
+@pytest.mark.parametrize("W", [1, 2, 4, 5, 6, 7, 8])
 def test_backward_model_other_widths(W):
     for (S, B, H) in [(1, 2, 384), (W + 1, 3, 1088), (300, 2, 640), (2049, 1, 2112)]:
         model_backward(S, B, H, W, m.PLAN_BWD_EX, full=True)
@@ -193,7 +236,7 @@ def test_backward_model_other_widths(W):
         model_backward(S, B, H, W, m.PLAN_BWD_EX, full=False)
 
 
-@pytest.mark.parametrize("W", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 6, 7, 8])
 def test_forward_model(W):
     for (S, B, H) in SMALL[:8]:
         model_forward(S, B, H, W, full=True)
