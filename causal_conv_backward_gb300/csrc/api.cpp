@@ -448,6 +448,7 @@ extern "C" int32_t mcc1d_plan_describe(int64_t S, int64_t B, int64_t H, int64_t 
     kv("red_splits", p.red_splits);
     kv("red_lanes", p.red_lanes);
     kv("regs_bound", kind == MCC1D_PLAN_FWD ? 0 : bwd_regs_bound(W));
+    kv("reg_split", p.reg_split);
     kv("long_ranges", long_ranges(p) ? 1 : 0);
     arr("c_lo", p.c_lo);
     arr("c_hi", p.c_hi);

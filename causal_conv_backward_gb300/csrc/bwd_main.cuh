@@ -53,7 +53,17 @@ __device__ __forceinline__ uint32_t stage_mask_byte(const MainParams &p, const C
     return __ldg(p.mask + (int64_t)c.j * p.m_b + row * p.m_s) != 0 ? 1u : 0u;
 }
 
-template <int R, int W>
+// The bounded wait, out of line unless the kernel splits its registers.
+template <int PT>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if constexpr (PT == kSplitProducerThreads)
+        return mbar_wait_bounded_inline(bar, parity);
+    else
+        return mbar_wait_bounded(bar, parity);
+}
+
+template <int R, int W, int PT>
 __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t r1, int lane)
 {
     const int NS = p.stages;
@@ -73,7 +83,7 @@ __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
         const bool head = (stage == 0) || (cur.i == 0);
         const uint32_t mcur = mnext;
         if (stage >= NS) {
-            const bool ok = mbar_wait_bounded(bar_empty0 + 8u * slot, ph ^ 1u);
+            const bool ok = wait_bounded<PT>(bar_empty0 + 8u * slot, ph ^ 1u);
             dead = __any_sync(0xFFFFFFFFu, !ok);
             if (dead)
                 break;
@@ -132,7 +142,7 @@ __device__ bool produce(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     const int used = stage < NS ? stage : NS;
     for (int s = 0; s < used; ++s) {
         const int last = s + NS * ((stage - 1 - s) / NS);
-        if (!mbar_wait_bounded(bar_full0 + 8u * s, (uint32_t)((last / NS) & 1)))
+        if (!wait_bounded<PT>(bar_full0 + 8u * s, (uint32_t)((last / NS) & 1)))
             dead = true;
     }
     return __any_sync(0xFFFFFFFFu, dead);
@@ -158,11 +168,11 @@ __device__ __forceinline__ Vf<NP> load_weight(const MainParams &p, int k, int64_
 
 // BS: gradX rows leave through the slot with bulk copies (4 KB rows over long
 // CTA ranges) instead of per-thread streaming stores.
-template <int DT, int R, int NP, int W, bool BS = false>
+template <int DT, int R, int NP, int W, bool BS, int PT>
 __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t r1, int ct, int lane)
 {
     const int NS = p.stages;
-    const int nct = (int)blockDim.x - 32;
+    const int nct = (int)blockDim.x - PT;                          // consumer threads
     const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
     constexpr int CH = 2 * NP;                                     // channels per thread
@@ -201,6 +211,13 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 #pragma unroll
         for (int e = 0; e < NP; ++e)
             win[q].e[e] = make_float2(0.f, 0.f);
+    // certified sums: kCert * max_k |w_k| per channel, and sum |gYm| over the
+    // window rows (both rounded up; the sum slides with the window and is
+    // recomputed at every stage, so its rounding does not build up)
+    float2 kmw[NP], gab[NP];
+#pragma unroll
+    for (int e = 0; e < NP; ++e)
+        kmw[e] = gab[e] = make_float2(0.f, 0.f);
 
     // Writes this thread's share of the partial for H-block hb_cur and clears
     // the accumulators. Sum order: shared-memory level, then register level.
@@ -251,11 +268,23 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 #pragma unroll
                 for (int k = 0; k < W; ++k)
                     wt[k] = load_weight<DT, NP>(p, k, hb0 + CH * ct);
+                if constexpr (kCF) {
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) {
+                        float mx = 0.f, my = 0.f;
+#pragma unroll
+                        for (int k = 0; k < W; ++k) {
+                            mx = fmaxf(mx, fabsf(wt[k].e[e].x));
+                            my = fmaxf(my, fabsf(wt[k].e[e].y));
+                        }
+                        kmw[e] = mul_ru(make_float2(kCert, kCert), make_float2(mx, my));
+                    }
+                }
             }
         }
         if (!dead) {
             const uint32_t bar = bar_full0 + 8u * slot;
-            const bool ok = mbar_try_wait(bar, ph) || mbar_wait_bounded(bar, ph);
+            const bool ok = mbar_try_wait(bar, ph) || wait_bounded<PT>(bar, ph);
             dead = __any_sync(0xFFFFFFFFu, !ok);
         }
         if (!dead && active) {
@@ -267,6 +296,16 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 #pragma unroll
                 for (int q = 0; q < WH; ++q)
                     win[q] = load_masked<DT, NP>(gys + (size_t)q * p.row_bytes, ms[q]);
+            }
+            if constexpr (kCF) {
+#pragma unroll
+                for (int e = 0; e < NP; ++e) {
+                    float2 g = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < WH; ++q)
+                        g = add_abs_ru(g, win[q].e[e]);
+                    gab[e] = g;
+                }
             }
             uint8_t *gxp = p.gx + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
             // gradWeight of this stage: W <= 3 sums the stage's R rows on
@@ -293,22 +332,20 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                     // gradX = sum_k gYm(i+k) w(W-1-k): exact fp32 products,
                     // a compensated sum, rounded once (sum_to16)
                     if constexpr (kCF) {
-                        // plain pairwise sum s of the exact products and the
-                        // sum a of their magnitudes in the same tree; when
-                        // kCert * a <= |s|, round(s) is within 1 ulp of the
-                        // exact sum rounded once (cert_factor); else the
-                        // channel is recomputed after the stage
-                        float2 pk[W], ak[W];
-#pragma unroll
-                        for (int k = 0; k < W; ++k) {
-                            pk[k] = mul2(k < WH ? win[k].e[e] : gn.e[e], wt[W - 1 - k].e[e]);
-                            ak[k] = abs2(pk[k]);
-                        }
-                        const float2 sf = tree_sum<0, W, W>(pk);
-                        const float2 af = tree_sum<0, W, W>(ak);
-                        const bool ok = (kCert * af.x <= fabsf(sf.x)) & (kCert * af.y <= fabsf(sf.y));
+                        // plain sum s of the exact products in a depth-3
+                        // tree; when kCert * max|w| * sum|gYm| (>= kCert *
+                        // sum|products|, rounded up) <= |s|, round(s) is
+                        // within 1 ulp of the exact sum rounded once
+                        // (cert_factor); else the channel is recomputed
+                        // after the stage
+                        const float2 gr = add_abs_ru(gab[e], gn.e[e]);
+                        const float2 sf = dot_tree<W>([&](int k) { return k < WH ? win[k].e[e] : gn.e[e]; },
+                                                      [&](int k) { return wt[W - 1 - k].e[e]; });
+                        const float2 lim = mul_ru(kmw[e], gr);
+                        const bool ok = (lim.x <= fabsf(sf.x)) & (lim.y <= fabsf(sf.y));
                         o[e] = pack2<DT>(sf);
                         fails |= (ok ? 0u : 1u) << (r * NP + e);
+                        gab[e] = sub_abs_ru(gr, win[0].e[e]);   // gYm(i+r) leaves the window
                     } else {
                         o[e] = sum_to16<DT, W>(
                             [&](int k) { return mul2(k < WH ? win[k].e[e] : gn.e[e], wt[W - 1 - k].e[e]); });
@@ -347,33 +384,29 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
                         row(r);
             }
             if constexpr (kCF) {
-                // channels whose certificate failed (a small fraction: strong
-                // cancellation): the cascade, from the staged rows; the rows
-                // before this stage are still in the previous slot, which is
-                // released one stage late for this
-                if (fails) {
-                    const uint8_t *psl = smem + (size_t)(prev_slot < 0 ? 0 : prev_slot) * p.slot_bytes + 2 * CH * ct;
-                    const uint8_t *pms = smem + p.off_mask + 32u * (prev_slot < 0 ? 0 : prev_slot);
-#pragma unroll 1
-                    for (int r = 0; r < n; ++r) {
+                // channels whose certificate failed (strong cancellation):
+                // the cascade, from the staged rows, one failed (row,
+                // channel pair) per iteration, each lane walking its own
+                // bits; the rows before this stage are still in the previous
+                // slot, which is released one stage late for this
+                const uint8_t *psl = smem + (size_t)(prev_slot < 0 ? 0 : prev_slot) * p.slot_bytes + 2 * CH * ct;
+                const uint8_t *pms = smem + p.off_mask + 32u * (prev_slot < 0 ? 0 : prev_slot);
+                while (fails) {
+                    const int b = __ffs(fails) - 1;
+                    fails &= fails - 1;
+                    const int r = b / NP, e = b % NP;
+                    float2 qk[W];
 #pragma unroll
-                        for (int e = 0; e < NP; ++e) {
-                            if ((fails >> (r * NP + e)) & 1u) {
-                                float2 qk[W];
-#pragma unroll
-                                for (int k = 0; k < W; ++k) {
-                                    const int q = r + k;
-                                    const bool here = head || q >= WH;
-                                    const uint8_t *rp = here ? gys + (size_t)q * p.row_bytes
-                                                             : psl + (size_t)(n_prev + q) * p.row_bytes;
-                                    const uint8_t mb = here ? ms[q] : pms[n_prev + q];
-                                    qk[k] = mul2(load_masked<DT, NP>(rp, mb).e[e], wt[W - 1 - k].e[e]);
-                                }
-                                const uint32_t v = sum_to16<DT, W>([&](int k) { return qk[k]; });
-                                *reinterpret_cast<uint32_t *>(gxp + (int64_t)r * row_stride + 4 * e) = v;
-                            }
-                        }
+                    for (int k = 0; k < W; ++k) {
+                        const int q = r + k;
+                        const bool here = head || q >= WH;
+                        const uint8_t *rp = here ? gys + (size_t)q * p.row_bytes
+                                                 : psl + (size_t)(n_prev + q) * p.row_bytes;
+                        const uint8_t mb = here ? ms[q] : pms[n_prev + q];
+                        qk[k] = mul2(load_masked_pair<DT>(rp + 4 * e, mb), pick_pair<NP>(wt[W - 1 - k], e));
                     }
+                    const uint32_t v = sum_to16<DT, W>([&](int k) { return qk[k]; });
+                    *reinterpret_cast<uint32_t *>(gxp + (int64_t)r * row_stride + 4 * e) = v;
                 }
             }
             if constexpr (kStageSums) {
@@ -445,7 +478,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
 }
 
 // ------------------------------------------------------------------ kernels
-template <int DT, int R, int NP, int W, bool BS>
+template <int DT, int R, int NP, int W, bool BS, int PT = 32>
 __device__ __forceinline__ void main_body(const MainParams &p)
 {
     // one producer lane per staged row (R + W - 1 gradY rows, R x rows), and
@@ -456,7 +489,7 @@ __device__ __forceinline__ void main_body(const MainParams &p)
     const int c = blockIdx.x;
     const int64_t r0 = cta_row_begin(c, p.N, p.ncta);
     const int64_t r1 = cta_row_begin(c + 1, p.N, p.ncta);
-    const int consumer_warps = (int)(blockDim.x >> 5) - 1;
+    const int consumer_warps = (int)((blockDim.x - PT) >> 5);
     if (threadIdx.x == 0) {
         s_err = 0;
         const uint32_t bar0 = smem_u32(smem + p.off_bar);
@@ -475,11 +508,19 @@ __device__ __forceinline__ void main_body(const MainParams &p)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int lane = threadIdx.x & 31;
-    bool dead;
-    if (threadIdx.x < 32)
-        dead = produce<R, W>(p, smem, r0, r1, lane);
-    else
-        dead = consume<DT, R, NP, W, BS>(p, smem, r0, r1, (int)threadIdx.x - 32, lane);
+    bool dead = false;
+    if (threadIdx.x < PT) {
+        // the register split (PT = 128): the producer's warpgroup gives up
+        // registers first, then the consumer warpgroups take them
+        if constexpr (PT == kSplitProducerThreads)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSplitProducerRegs));
+        if (threadIdx.x < 32)
+            dead = produce<R, W, PT>(p, smem, r0, r1, lane);
+    } else {
+        if constexpr (PT == kSplitProducerThreads)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSplitConsumerRegs));
+        dead = consume<DT, R, NP, W, BS, PT>(p, smem, r0, r1, (int)threadIdx.x - PT, lane);
+    }
     if (dead && lane == 0)
         atomicOr(&s_err, 1);
     __syncthreads();
@@ -505,6 +546,15 @@ template <int DT, int R, int NP, int W>
 __global__ void __launch_bounds__(kMaxThreads, 2) mcc1d_bwd_main_x2(const __grid_constant__ MainParams p)
 {
     main_body<DT, R, NP, W, false>(p);
+}
+
+// The widest kernels with the register file split by warpgroup: the
+// producer's warpgroup (one producing warp, three idle) at 56 registers, the
+// consumer warpgroups at 224, from a launch at 168 per thread (384 threads).
+template <int DT, int R, int NP, int W>
+__global__ void __launch_bounds__(kSplitMaxThreads, 1) mcc1d_bwd_main_rs(const __grid_constant__ MainParams p)
+{
+    main_body<DT, R, NP, W, false, kSplitProducerThreads>(p);
 }
 
 typedef void (*MainFn)(MainParams);

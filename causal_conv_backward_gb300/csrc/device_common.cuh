@@ -56,7 +56,7 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 
 // Waits for the phase of `bar` with the given parity to complete; gives up
 // (returns false) after kWaitLimitNs.
-static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait_bounded_inline(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -67,6 +67,14 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t par
         if (global_timer_ns() - t0 > kWaitLimitNs)
             return false;
     }
+}
+
+// The same, out of line (keeps the slow path out of the hot loops). Kernels
+// that split their registers by warpgroup (setmaxnreg) take the inline form:
+// one out-of-line body cannot serve regions of different register counts.
+static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    return mbar_wait_bounded_inline(bar, parity);
 }
 
 // Global -> shared bulk copy completing on an mbarrier (no multicast).
@@ -227,6 +235,25 @@ __device__ __forceinline__ Vf<NP> load_masked(const uint8_t *p, uint8_t keep_byt
     return unpack<DT, NP>(r);
 }
 
+// One channel pair (4 bytes) of a staged row, masked like load_masked.
+template <int DT>
+__device__ __forceinline__ float2 load_masked_pair(const uint8_t *p, uint8_t keep_byte)
+{
+    return unpack2<DT>(*reinterpret_cast<const uint32_t *>(p) & (0u - (uint32_t)keep_byte));
+}
+
+// Channel pair e of v, e a run-time index (selects, no local memory).
+template <int NP>
+__device__ __forceinline__ float2 pick_pair(const Vf<NP> &v, int e)
+{
+    float2 r = v.e[0];
+#pragma unroll
+    for (int t = 1; t < NP; ++t)
+        if (e == t)
+            r = v.e[t];
+    return r;
+}
+
 // ------------------------------------------------------------------ sums of W products
 // The gradX (and forward y) value of a channel is a sum of W products of two
 // 16-bit values. Each product is exact in fp32 (8 x 8 or 11 x 11 significant
@@ -259,46 +286,66 @@ __device__ __forceinline__ uint32_t sum_to16(Prod prod)
         return pack2<DT>(s);
 }
 
-// |v| of both lanes (clears the sign bits).
-__device__ __forceinline__ float2 abs2(float2 v)
+// s = sum_k a(k) b(k) for W <= 8 in a fixed tree of depth <= 3: each pair
+// a(2j) b(2j) + a(2j+1) b(2j+1) by one multiply and one fused multiply-add
+// (products of two 16-bit values are exact in fp32, so a pair rounds once),
+// then the pairs' tree; an odd last product is fused into the last pair.
+template <int W, typename A, typename B>
+__device__ __forceinline__ float2 dot_tree(A a, B b)
 {
-    return make_float2(__uint_as_float(__float_as_uint(v.x) & 0x7FFFFFFFu),
-                       __uint_as_float(__float_as_uint(v.y) & 0x7FFFFFFFu));
-}
-
-// Pairwise sum of v[LO .. LO+N) in a fixed tree: the first half is the
-// largest power of two below N, so no element passes more than ceil(log2 N)
-// additions.
-template <int LO, int N, int W>
-__device__ __forceinline__ float2 tree_sum(const float2 (&v)[W])
-{
-    if constexpr (N == 1) {
-        return v[LO];
+    static_assert(W >= 1 && W <= 8, "the depth-3 tree holds up to 8 products");
+    if constexpr (W == 1) {
+        return mul2(a(0), b(0));
     } else {
-        constexpr int kHalf = N > 4 ? 4 : (N > 2 ? 2 : 1);
-        return add2(tree_sum<LO, kHalf, W>(v), tree_sum<LO + kHalf, N - kHalf, W>(v));
+        constexpr int kPairs = W / 2;
+        float2 pr[kPairs];
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j)
+            pr[j] = fma2(a(2 * j + 1), b(2 * j + 1), mul2(a(2 * j), b(2 * j)));
+        if constexpr (W & 1)
+            pr[kPairs - 1] = fma2(a(W - 1), b(W - 1), pr[kPairs - 1]);
+        if constexpr (kPairs == 1)
+            return pr[0];
+        else if constexpr (kPairs == 2)
+            return add2(pr[0], pr[1]);
+        else if constexpr (kPairs == 3)
+            return add2(add2(pr[0], pr[1]), pr[2]);
+        else
+            return add2(add2(pr[0], pr[1]), add2(pr[2], pr[3]));
     }
 }
 
-// Certificate for a pairwise sum s of W <= 8 exact products (tree depth 3)
-// whose magnitudes sum to a (same tree): |s - exact| <= gamma_3 * sum|p| <=
+// Upper bounds, per lane, by rounding toward +infinity: s + |v|, s - |v|,
+// a * b.
+__device__ __forceinline__ float2 add_abs_ru(float2 s, float2 v)
+{
+    return make_float2(__fadd_ru(s.x, fabsf(v.x)), __fadd_ru(s.y, fabsf(v.y)));
+}
+__device__ __forceinline__ float2 sub_abs_ru(float2 s, float2 v)
+{
+    return make_float2(__fsub_ru(s.x, fabsf(v.x)), __fsub_ru(s.y, fabsf(v.y)));
+}
+__device__ __forceinline__ float2 mul_ru(float2 a, float2 b)
+{
+    return make_float2(__fmul_ru(a.x, b.x), __fmul_ru(a.y, b.y));
+}
+
+// Certificate for a sum s of W <= 8 exact products p_k = g_k w_k in a tree
+// of depth 3 (dot_tree): with a = sum_k |p_k|, |s - exact| <= gamma_3 * a <=
 // 3u(1 + 4u) a (Higham, "Accuracy and Stability of Numerical Algorithms",
 // 2nd ed., section 4.2; u = 2^-24). The 16-bit grid's spacing at x exceeds
 // x * 2^-(m+1) (m + 1 significant bits: 11 for fp16, 8 for bf16), so if
 // that error bound is below (|s| - bound) * 2^-(m+1), s and the exact sum lie
 // closer than the smallest spacing between them: at most one rounding
 // boundary separates them and round(s) is within 1 ulp of the exact sum
-// rounded once. The test kCert * a <= |s| implies this, with slack for the
-// roundings of a and of the product.
+// rounded once. The kernels test kCert * max_k|w_k| * sum_k|g_k| <= |s|,
+// whose left side, formed with upward rounding, is at least kCert * a, so
+// the factor's last (1 + 2^-20) is margin.
 constexpr int kCertMinW = 6;
-// Where the certified sum replaces the cascade: bf16 from W = 6 (below that
-// the kernels are not bound by their sums); fp16 at W = 8 only. fp16 has 10
-// fraction bits to bf16's 7, so its certificate is 8x tighter and fails about
-// 8x as often on the same data; a warp with one failing lane pays the whole
-// recompute, and at W = 6, 7 the cascade measured faster.
+// Where the certified sum replaces the cascade.
 __host__ __device__ constexpr bool cert_uses_plain_sum(int DT, int W)
 {
-    return W >= kCertMinW && (DT == 0 || W == 8);
+    return W >= kCertMinW && DT >= 0;
 }
 template <int DT>
 __host__ __device__ constexpr float cert_factor()

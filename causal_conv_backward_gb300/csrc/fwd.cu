@@ -203,6 +203,12 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
 #pragma unroll
         for (int e = 0; e < NP; ++e)
             win[q].e[e] = make_float2(0.f, 0.f);
+    // certified sums: kCert * max_k |w_k| per channel, and sum |x| over the
+    // window rows (both rounded up; recomputed at every stage)
+    float2 kmw[NP], gab[NP];
+#pragma unroll
+    for (int e = 0; e < NP; ++e)
+        kmw[e] = gab[e] = make_float2(0.f, 0.f);
     int slot = 0, stage = 0;
     uint32_t ph = 0;
     bool dead = false;
@@ -219,6 +225,18 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
 #pragma unroll
                 for (int k = 0; k < W; ++k)
                     wt[k] = fwd_weight<DT, NP>(p, k, hb0 + CH * ct);
+                if constexpr (kCF) {
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) {
+                        float mx = 0.f, my = 0.f;
+#pragma unroll
+                        for (int k = 0; k < W; ++k) {
+                            mx = fmaxf(mx, fabsf(wt[k].e[e].x));
+                            my = fmaxf(my, fabsf(wt[k].e[e].y));
+                        }
+                        kmw[e] = mul_ru(make_float2(kCert, kCert), make_float2(mx, my));
+                    }
+                }
             }
         }
         if (!dead) {
@@ -237,6 +255,16 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                 for (int q = 0; q < WH; ++q)
                     win[q] = load_masked<DT, NP>(hs + (size_t)q * p.row_bytes, ms[q]);
             }
+            if constexpr (kCF) {
+#pragma unroll
+                for (int e = 0; e < NP; ++e) {
+                    float2 g = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < WH; ++q)
+                        g = add_abs_ru(g, win[q].e[e]);
+                    gab[e] = g;
+                }
+            }
             uint8_t *yp = p.y + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
             uint32_t fails = 0;
             auto row = [&](int r) {
@@ -246,20 +274,17 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
 #pragma unroll
                 for (int e = 0; e < NP; ++e) {
                     if constexpr (kCF) {
-                        // plain pairwise sums of the exact products and of
-                        // their magnitudes; kept when kCert * a <= |s|
-                        // (within 1 ulp of the exact sum rounded once)
-                        float2 pk[W], ak[W];
-#pragma unroll
-                        for (int k = 0; k < W; ++k) {
-                            pk[k] = mul2(k < WH ? win[k].e[e] : xn.e[e], wt[k].e[e]);
-                            ak[k] = abs2(pk[k]);
-                        }
-                        const float2 sf = tree_sum<0, W, W>(pk);
-                        const float2 af = tree_sum<0, W, W>(ak);
-                        const bool ok = (kCert * af.x <= fabsf(sf.x)) & (kCert * af.y <= fabsf(sf.y));
+                        // plain sum of the exact products in a depth-3 tree,
+                        // kept when kCert * max|w| * sum|x| (rounded up) <=
+                        // |s| (within 1 ulp of the exact sum rounded once)
+                        const float2 gr = add_abs_ru(gab[e], xn.e[e]);
+                        const float2 sf = dot_tree<W>([&](int k) { return k < WH ? win[k].e[e] : xn.e[e]; },
+                                                      [&](int k) { return wt[k].e[e]; });
+                        const float2 lim = mul_ru(kmw[e], gr);
+                        const bool ok = (lim.x <= fabsf(sf.x)) & (lim.y <= fabsf(sf.y));
                         o[e] = pack2<DT>(sf) & keep;
                         fails |= (ok ? 0u : 1u) << (r * NP + e);
+                        gab[e] = sub_abs_ru(gr, win[0].e[e]);   // x(t+r-W+1) leaves the window
                     } else {
                         // exact fp32 products, summed and rounded once by
                         // sum_to16 (the backward's gradX sum)
@@ -296,36 +321,29 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
             }
             if constexpr (kCF) {
                 // failed channels (strong cancellation): the cascade over
-                // x(t+r-W+1) .. x(t+r), from this slot, the halo area at a
-                // head stage, else the previous slot (released one stage
-                // late for this); the stored value is overwritten
-                if (fails) {
-                    const uint8_t *hs = smem + p.off_halo + 2 * CH * ct;
-                    const uint8_t *psl = smem + (size_t)(prev_slot < 0 ? 0 : prev_slot) * p.slot_bytes + 2 * CH * ct;
-#pragma unroll 1
-                    for (int r = 0; r < n; ++r) {
-                        const uint32_t keep = 0u - (uint32_t)ms[r + WH];
+                // x(t+r-W+1) .. x(t+r), one failed (row, channel pair) per
+                // iteration, from this slot, the halo area at a head stage,
+                // else the previous slot (released one stage late for
+                // this); the stored value is overwritten
+                const uint8_t *hs = smem + p.off_halo + 2 * CH * ct;
+                const uint8_t *psl = smem + (size_t)(prev_slot < 0 ? 0 : prev_slot) * p.slot_bytes + 2 * CH * ct;
+                while (fails) {
+                    const int b = __ffs(fails) - 1;
+                    fails &= fails - 1;
+                    const int r = b / NP, e = b % NP;
+                    float2 qk[W];
 #pragma unroll
-                        for (int e = 0; e < NP; ++e) {
-                            if ((fails >> (r * NP + e)) & 1u) {
-                                float2 qk[W];
-#pragma unroll
-                                for (int k = 0; k < W; ++k) {
-                                    const int d = r + k - WH;   // x row relative to the stage's first
-                                    Vf<NP> xv;
-                                    if (d >= 0)
-                                        xv = unpack<DT, NP>(load_raw<NP>(xs + (size_t)d * p.row_bytes));
-                                    else if (head)
-                                        xv = load_masked<DT, NP>(hs + (size_t)(WH + d) * p.row_bytes, ms[WH + d]);
-                                    else
-                                        xv = unpack<DT, NP>(load_raw<NP>(psl + (size_t)(n_prev + d) * p.row_bytes));
-                                    qk[k] = mul2(xv.e[e], wt[k].e[e]);
-                                }
-                                const uint32_t v = sum_to16<DT, W>([&](int k) { return qk[k]; }) & keep;
-                                *reinterpret_cast<uint32_t *>(yp + (int64_t)r * row_stride + 4 * e) = v;
-                            }
-                        }
+                    for (int k = 0; k < W; ++k) {
+                        const int d = r + k - WH;   // x row relative to the stage's first
+                        const uint8_t *rp = d >= 0 ? xs + (size_t)d * p.row_bytes
+                                          : head   ? hs + (size_t)(WH + d) * p.row_bytes
+                                                   : psl + (size_t)(n_prev + d) * p.row_bytes;
+                        const uint8_t mb = (d < 0 && head) ? ms[WH + d] : (uint8_t)1;
+                        qk[k] = mul2(load_masked_pair<DT>(rp + 4 * e, mb), pick_pair<NP>(wt[k], e));
                     }
+                    const uint32_t keep = 0u - (uint32_t)ms[r + WH];
+                    const uint32_t v = sum_to16<DT, W>([&](int k) { return qk[k]; }) & keep;
+                    *reinterpret_cast<uint32_t *>(yp + (int64_t)r * row_stride + 4 * e) = v;
                 }
             }
         }

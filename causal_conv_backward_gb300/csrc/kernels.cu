@@ -180,15 +180,53 @@ static MainFn main_for(int R, bool bulk)
 }
 
 // Instances for W != 3 live in kernels_w.cu.
-MainFn main_kernel_other_w(int dtype, int vec, int W, int R);
+MainFn main_kernel_other_w(int dtype, int vec, int W, int R, bool split);
 
-static MainFn main_kernel(int dtype, int R, int vec, int W, bool bulk)
+static MainFn main_kernel(int dtype, int R, int vec, int W, bool bulk, bool split)
 {
     if (W != 3)
-        return bulk ? nullptr : main_kernel_other_w(dtype, vec, W, R);
+        return bulk ? nullptr : main_kernel_other_w(dtype, vec, W, R, split);
+    if (split)
+        return nullptr;
     if (dtype == 0)
         return vec == 4 ? main_for<0, 2>(R, bulk) : main_for<0, 4>(R, bulk);
     return vec == 4 ? main_for<1, 2>(R, bulk) : main_for<1, 4>(R, bulk);
+}
+
+// A kernel that splits its registers by warpgroup (setmaxnreg) is launched
+// only when the registers the CTA starts with cover what its warpgroups hold
+// after the split: the consumers' increase draws on what the producer's
+// warpgroup gives up, and would otherwise wait for registers that never come.
+static bool split_fits(const void *fn, int threads)
+{
+    constexpr int kSlots = 16;
+    static std::mutex mu;
+    static const void *fns[kSlots];
+    static int regs[kSlots];
+    if (threads % kSplitProducerThreads != 0 || threads <= kSplitProducerThreads || threads > kSplitMaxThreads)
+        return false;
+    int r = -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < kSlots && fns[i]; ++i)
+            if (fns[i] == fn)
+                r = regs[i];
+        if (r < 0) {
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess)
+                return false;
+            r = fa.numRegs;
+            for (int i = 0; i < kSlots; ++i)
+                if (!fns[i]) {
+                    fns[i] = fn;
+                    regs[i] = r;
+                    break;
+                }
+        }
+    }
+    const int64_t need = (int64_t)kSplitProducerThreads * kSplitProducerRegs +
+                         (int64_t)(threads - kSplitProducerThreads) * kSplitConsumerRegs;
+    return (int64_t)r * threads >= need;
 }
 
 // gradX leaves by bulk copies out of the ring on 4 KB rows (8 channels per
@@ -334,10 +372,12 @@ int32_t launch_bwd(const Plan &pl, const Layout &L, const void *gradY, const voi
     mp.w_vec = (L.w[1] == 1 && (L.w[0] * 2) % 16 == 0 && ((uintptr_t)weight & 15u) == 0) ? 1 : 0;
 
     const int R = pl.rows_per_stage;
-    MainFn mfn = main_kernel(pl.dtype, R, pl.vec, pl.W, bwd_bulk_store(pl));
+    MainFn mfn = main_kernel(pl.dtype, R, pl.vec, pl.W, bwd_bulk_store(pl), pl.reg_split != 0);
     if (!mfn)
         return kErrCuda;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(mfn)))
+        return kErrCuda;
+    if (pl.reg_split && !split_fits(reinterpret_cast<const void *>(mfn), pl.threads))
         return kErrCuda;
 
     cudaLaunchConfig_t cfg = {};

@@ -1,45 +1,55 @@
 // kernels_w.cu - instances of the backward's main kernel for widths W other
-// than 3 (one rows-per-stage choice, R = 6; R = 8 at W = 8), for the strided entry points,
-// which accept 1 <= W <= 8. Widths from 4 up keep 4 channels per thread so
-// their W accumulators per channel stay in registers; widths 4 and 5 run two
-// CTAs per SM under the matching register bound. Compiled apart from
-// kernels.cu so the two build in parallel.
+// than 3 (one rows-per-stage choice, R = 6; R = 8 at W = 8), for the strided
+// entry points, which accept 1 <= W <= 8. Widths from 4 up keep 4 channels
+// per thread so their W accumulators per channel stay in registers; widths 4
+// and 5 run two CTAs per SM under the matching register bound; widths from 6
+// split the register file by warpgroup when an H-block needs more than one
+// consumer warpgroup (mcc1d_bwd_main_rs), else run the plain one-CTA form.
+// Compiled apart from kernels.cu so the two build in parallel.
 #include "bwd_main.cuh"
 
 namespace mcc1d {
 
 template <int DT, int W>
-static MainFn pick(int vec, int R)
+static MainFn pick(int vec, int R, bool split)
 {
-    if constexpr (W == kMaxW)
-        return vec == 4 && R == 8 ? mcc1d_bwd_main<DT, 8, 2, W> : nullptr;
-    else if constexpr (W >= 4 && W <= kTwoCtaMaxW)
-        return vec == 4 && R == 6 ? mcc1d_bwd_main_x2<DT, 6, 2, W> : nullptr;
-    else if constexpr (W >= 4)
-        return vec == 4 && R == 6 ? mcc1d_bwd_main<DT, 6, 2, W> : nullptr;
-    else if (R == 6)
-        return vec == 4 ? mcc1d_bwd_main<DT, 6, 2, W> : mcc1d_bwd_main<DT, 6, 4, W>;
-    return nullptr;
+    constexpr int kR = W == kMaxW ? 8 : 6;
+    if (R != kR)
+        return nullptr;
+    if constexpr (W >= kSplitMinW) {
+        if (vec != 4)
+            return nullptr;
+        return split ? mcc1d_bwd_main_rs<DT, kR, 2, W> : mcc1d_bwd_main<DT, kR, 2, W>;
+    } else {
+        if (split)
+            return nullptr;
+        if constexpr (W >= 4 && W <= kTwoCtaMaxW)
+            return vec == 4 ? mcc1d_bwd_main_x2<DT, 6, 2, W> : nullptr;
+        else if constexpr (W >= 4)
+            return vec == 4 ? mcc1d_bwd_main<DT, 6, 2, W> : nullptr;
+        else
+            return vec == 4 ? mcc1d_bwd_main<DT, 6, 2, W> : mcc1d_bwd_main<DT, 6, 4, W>;
+    }
 }
 
 template <int DT>
-static MainFn pick_w(int vec, int W, int R)
+static MainFn pick_w(int vec, int W, int R, bool split)
 {
     switch (W) {
-    case 1: return pick<DT, 1>(vec, R);
-    case 2: return pick<DT, 2>(vec, R);
-    case 4: return pick<DT, 4>(vec, R);
-    case 5: return pick<DT, 5>(vec, R);
-    case 6: return pick<DT, 6>(vec, R);
-    case 7: return pick<DT, 7>(vec, R);
-    case 8: return pick<DT, 8>(vec, R);
+    case 1: return pick<DT, 1>(vec, R, split);
+    case 2: return pick<DT, 2>(vec, R, split);
+    case 4: return pick<DT, 4>(vec, R, split);
+    case 5: return pick<DT, 5>(vec, R, split);
+    case 6: return pick<DT, 6>(vec, R, split);
+    case 7: return pick<DT, 7>(vec, R, split);
+    case 8: return pick<DT, 8>(vec, R, split);
     default: return nullptr;
     }
 }
 
-MainFn main_kernel_other_w(int dtype, int vec, int W, int R)
+MainFn main_kernel_other_w(int dtype, int vec, int W, int R, bool split)
 {
-    return dtype == 0 ? pick_w<0>(vec, W, R) : pick_w<1>(vec, W, R);
+    return dtype == 0 ? pick_w<0>(vec, W, R, split) : pick_w<1>(vec, W, R, split);
 }
 
 }  // namespace mcc1d

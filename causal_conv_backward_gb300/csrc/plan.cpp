@@ -50,7 +50,9 @@ int32_t make_plan_general(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dt
     // the longer arithmetic of each row.
     if (W >= 4)
         return make_plan_for(S, B, H, W, dtype,
-                             {W <= kTwoCtaMaxW ? 16 : 8, kHbWidthNarrow, bwd_regs_bound(W), 5, false}, p);
+                             {W <= kTwoCtaMaxW ? 16 : 8, kHbWidthNarrow, bwd_regs_bound(W), 5, false,
+                              bwd_reg_split(W)},
+                             p);
     const int32_t st = make_plan_for(S, B, H, W, dtype, {8, kHbWidthWide, bwd_regs_bound(W), 5, false}, p);
     if (st != kOk || p->rows_total / p->ncta >= kWideMinRowsPerCta)
         return st;
@@ -97,6 +99,13 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     const int vectors = p->hb_width / p->vec;
     p->consumer_warps = (int32_t)ceil_div(vectors, 32);
     p->threads = 32 * (p->consumer_warps + 1);
+    p->reg_split = (o.reg_split && p->consumer_warps >= kSplitMinConsumerWarps) ? 1 : 0;
+    if (p->reg_split) {
+        // whole consumer warpgroups behind the producer's warpgroup (the
+        // extra warps own no channels)
+        p->consumer_warps = (int32_t)round_up(p->consumer_warps, 4);
+        p->threads = kSplitProducerThreads + 32 * p->consumer_warps;
+    }
 
     // Aim for at least target_consumer_warps consumer warps per SM.
     int cps = (int)ceil_div(target_consumer_warps, p->consumer_warps);

@@ -23,6 +23,28 @@ constexpr int kMaxW = 8;              // widest kernel the strided entry points 
 constexpr int kTwoCtaMaxW = 5;        // widths 4 .. kTwoCtaMaxW run two CTAs per SM
 constexpr int kRegsOneCta = 168;      // register bound of the main kernel (288 threads, one CTA)
 constexpr int kRegsTwoCta = 96;       // ... and of its two-CTA form (mcc1d_bwd_main_x2)
+// From W = kSplitMinW the backward's main kernel splits the register file by
+// warpgroup (mcc1d_bwd_main_rs): launched at kSplitLaunchRegs per thread, the
+// producer's warpgroup (kSplitProducerThreads threads, one warp of them
+// producing) drops to kSplitProducerRegs and the consumer warpgroups rise to
+// kSplitConsumerRegs. The consumers' share must come from what the producer
+// group gives up: 128 * 56 + 256 * 224 = 384 * 168 exactly at the widest
+// plan (8 consumer warps), less for narrower ones.
+constexpr int kSplitMinW = 6;
+constexpr int kSplitProducerThreads = 128;
+constexpr int kSplitLaunchRegs = 168;
+constexpr int kSplitProducerRegs = 56;
+constexpr int kSplitConsumerRegs = 224;
+constexpr int kSplitMaxThreads = 384;
+// Only H-blocks that need more than one consumer warpgroup split: narrower
+// ones (at most 512 channels) would pad to a whole warpgroup behind a
+// 4-warp producer group and fit one CTA per SM instead of three.
+constexpr int kSplitMinConsumerWarps = 5;
+static_assert(kSplitProducerThreads * kSplitProducerRegs +
+                      (kSplitMaxThreads - kSplitProducerThreads) * kSplitConsumerRegs <=
+                  kSplitMaxThreads * kSplitLaunchRegs,
+              "the register split must fit the launch's registers");
+inline bool bwd_reg_split(int64_t W) { return W >= kSplitMinW; }
 constexpr int kDeepMinRowsPerCta = 256;  // CTA range long enough for 14-row stages
 constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs (MCC1D_PLAN_SMS; checked per device)
 constexpr int kSmemPerSM = 233472;    // 228 KB of shared memory per SM
@@ -66,6 +88,7 @@ struct Plan {
     // or 4: an 8-byte vector) of the H-block.
     int32_t vec;
     int32_t consumer_warps, threads;
+    int32_t reg_split;       // 1: the main kernel splits its registers by warpgroup
     int32_t rows_per_stage;  // R: rows of x (and R+W-1 of gradY) per ring slot
     int32_t stages;          // ring slots
     int32_t ctas_per_sm;
@@ -134,6 +157,7 @@ struct PlanOpts {
                                  // never exceed what the register file holds (0: no cap)
     int vec4_max_warps;          // 4 channels per thread allowed up to this many consumer warps
     bool vec4_always;            // ... and taken whenever allowed (else only for better lane use)
+    bool reg_split = false;      // producer warpgroup + whole consumer warpgroups (setmaxnreg)
 };
 int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, const PlanOpts &o,
                       Plan *p);

@@ -1,18 +1,20 @@
-"""The certificate of the backward's plain gradX sum at widths 6..8.
+"""The certificate of the wide kernels' plain sum (widths 6..8).
 
-At W >= 6 the backward's main kernel sums the W exact fp32 products of a
-gradX value in a fixed pairwise tree and keeps the result when
-cert_factor * (the same tree over |products|) <= |sum|; otherwise the channel
-is recomputed with the compensated cascade. The claim is that every kept
-value, rounded once to the 16-bit type, is within 1 ulp of the exact sum
-rounded once (the acceptance bar of the page's gradX).
+At W >= 6 the backward's and the forward's main kernels sum the W exact fp32
+products of a value in a fixed tree of depth 3 (pairs by a multiply and a
+fused multiply-add, then the pairs' tree) and keep the result when
+cert_factor * max_k|w_k| * sum_k|g_k| (formed with upward rounding) <= |sum|;
+otherwise the channel is recomputed with the compensated cascade. The claim
+is that every kept value, rounded once to the 16-bit type, is within 1 ulp of
+the exact sum rounded once (the acceptance bar of the page's gradX).
 
 These CPU tests check the claim by simulation, independently of the kernel's
 build: the factors in device_common.cuh are read as text and compared with
-the bound they rest on, and the fp32 tree (IEEE round-to-nearest additions,
-as add.rn.f32x2 does) runs in numpy on seeded inputs built for heavy
-cancellation, where the certificate is tight. Exact sums come from float64,
-exact here because the inputs span a narrow exponent range.
+the bound they rest on, and the fp32 tree (IEEE round-to-nearest additions;
+a fused multiply-add of two exact products rounds once, as a float32 add of
+them does) runs in numpy on seeded inputs built for heavy cancellation, where
+the certificate is tight. Exact sums come from float64, exact here because
+the inputs span a narrow exponent range.
 """
 import os
 import re
@@ -48,8 +50,8 @@ def header_factors():
 def needed_factor(mbits):
     """Smallest factor the argument accepts: gamma_3 (three roundings of
     u = 2^-24 on any path of a depth-3 tree) against half the 16-bit
-    relative spacing 2^-(m+1), with the distance |s| - bound, and a little for
-    the roundings of the magnitude sum and of the factor's product."""
+    relative spacing 2^-(m+1), with the distance |s| - bound; the last
+    (1 + 2^-20) is margin (the kernels form their bound with upward rounding)."""
     u = 2.0 ** -24
     gamma3 = 3 * u / (1 - 3 * u)
     return gamma3 * 2.0 ** (mbits + 1) / (1 - 2.0 ** -mbits) * (1 + 2.0 ** -20)
@@ -85,14 +87,30 @@ def ulp16(x, dt):
 
 
 def tree(v):
-    """The kernel's pairwise tree over v[..., 0:W] in float32: halves of 4,
-    2, 1 (W = 6: (01 + 23) + 45; 7: (01 + 23) + (45 + 6); 8: (01 + 23) + (45 + 67))."""
-    def rec(lo, n):
-        if n == 1:
-            return v[:, lo]
-        half = 4 if n > 4 else (2 if n > 2 else 1)
-        return (rec(lo, half) + rec(lo + half, n - half)).astype(np.float32)
-    return rec(0, v.shape[1])
+    """The kernels' dot_tree over exact products v[..., 0:W] in float32:
+    pairs (2j, 2j+1) rounded once, an odd last product fused into the last
+    pair, then the pairs' tree (W = 6: (P0 + P1) + P2; 7: (P0 + P1) + (P2 + p6);
+    8: (P0 + P1) + (P2 + P3))."""
+    f = np.float32
+    W = v.shape[1]
+    pr = [(v[:, 2 * j] + v[:, 2 * j + 1]).astype(f) for j in range(W // 2)]
+    if W % 2:
+        pr[-1] = (pr[-1] + v[:, W - 1]).astype(f)
+    if len(pr) == 1:
+        return pr[0]
+    if len(pr) == 2:
+        return (pr[0] + pr[1]).astype(f)
+    if len(pr) == 3:
+        return ((pr[0] + pr[1]).astype(f) + pr[2]).astype(f)
+    return ((pr[0] + pr[1]).astype(f) + (pr[2] + pr[3]).astype(f)).astype(f)
+
+
+def up32(x):
+    """float64 x -> the smallest float32 >= x (rounding toward +infinity)."""
+    r = x.astype(np.float32)
+    lo = r.astype(np.float64) < x
+    r[lo] = np.nextafter(r[lo], np.float32(np.inf))
+    return r
 
 
 def operands(rng, n, W, dt, cancel):
@@ -123,8 +141,13 @@ def test_every_certified_sum_is_within_one_ulp(dt, W):
         p64 = g.astype(np.float64) * w.astype(np.float64)
         assert np.array_equal(p32.astype(np.float64), p64)
         s = tree(p32)
-        a = tree(np.abs(p32))
-        ok = (cert * a).astype(np.float32) <= np.abs(s)
+        # kCert * max|w| and sum|g|, each rounded up, and their product
+        # rounded up: the kernels' bound, at least kCert * sum|products|
+        kmw = up32(np.float64(cert) * np.abs(w).max(1).astype(np.float64))
+        gs = up32(np.abs(g).astype(np.float64).sum(1))
+        lim = up32(kmw.astype(np.float64) * gs.astype(np.float64))
+        assert np.all(lim.astype(np.float64) >= np.float64(cert) * np.abs(p64).sum(1))
+        ok = lim <= np.abs(s)
         exact = p64.sum(1)                                   # exact: narrow exponent range
         nz = exact != 0
         ok &= nz

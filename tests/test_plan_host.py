@@ -39,8 +39,18 @@ def check_common(p, S, B, H, W):
     assert hbw % 64 == 0 and 1 <= nhb <= 64
     assert nhb * hbw >= H and (nhb - 1) * hbw < H
     assert p["vec"] in (4, 8)
-    assert p["consumer_warps"] == cdiv(hbw // p["vec"], 32)
-    assert p["threads"] == 32 * (p["consumer_warps"] + 1) <= MAX_THREADS
+    if p.get("reg_split"):
+        # whole consumer warpgroups behind the producer's warpgroup, and the
+        # register split (setmaxnreg: producer group 56, consumers 224)
+        # within the registers the CTA is launched with (168 per thread)
+        assert p["consumer_warps"] == 4 * cdiv(cdiv(hbw // p["vec"], 32), 4)
+        assert p["threads"] == 128 + 32 * p["consumer_warps"] <= 384
+        assert 168 * p["threads"] >= 56 * 128 + 224 * (p["threads"] - 128)
+        # and per scheduler: at most one producer-group warp and two consumer warps
+        assert 56 * 32 + 2 * 224 * 32 <= 16384
+    else:
+        assert p["consumer_warps"] == cdiv(hbw // p["vec"], 32)
+        assert p["threads"] == 32 * (p["consumer_warps"] + 1) <= MAX_THREADS
     assert p["row_bytes"] == 2 * hbw and p["row_bytes"] % 16 == 0
     assert p["stages"] >= 2
     cps = p["ctas_per_sm"]
@@ -70,6 +80,7 @@ def check_bwd(p, S, B, H, W):
     R = p["rows_per_stage"]
     assert R in ((4, 6, 8, 14) if W == 3 else (8,) if W == 8 else (6,))
     assert W < 6 or W - 1 <= R        # the certified sum's fallback reads the previous slot
+    assert p["reg_split"] == (1 if W >= 6 and cdiv(p["hb_width"] // p["vec"], 32) > 4 else 0)
     assert R != 14 or p["vec"] == 4
     assert 2 * R + W - 1 <= 32               # one producer lane per staged row
     assert p["slot_bytes"] == (2 * R + W - 1) * p["row_bytes"]
