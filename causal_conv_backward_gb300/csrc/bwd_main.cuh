@@ -178,9 +178,9 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     constexpr int CH = 2 * NP;                                     // channels per thread
     constexpr int WH = W - 1;                                      // rows of the window
     constexpr bool kStageSums = W <= 3;                            // per-stage gradWeight level
-    // Wide kernels (cert_uses_plain_sum): gradX by a certified plain sum,
-    // the cascade only where the certificate fails (see below).
-    constexpr bool kCF = cert_uses_plain_sum(DT, W) && !BS;
+    // Wide kernels (kCertMinWBwd): gradX by a certified plain sum, the
+    // cascade only where the certificate fails (see below).
+    constexpr bool kCF = W >= kCertMinWBwd && !BS;
     constexpr float kCert = cert_factor<DT>();
     // the fallback finds the W-1 rows before a stage in the previous slot,
     // whose look-ahead holds R rows; one failure bit per (row, channel pair)

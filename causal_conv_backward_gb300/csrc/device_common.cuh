@@ -341,12 +341,12 @@ __device__ __forceinline__ float2 mul_ru(float2 a, float2 b)
 // rounded once. The kernels test kCert * max_k|w_k| * sum_k|g_k| <= |s|,
 // whose left side, formed with upward rounding, is at least kCert * a, so
 // the factor's last (1 + 2^-20) is margin.
-constexpr int kCertMinW = 6;
-// Where the certified sum replaces the cascade.
-__host__ __device__ constexpr bool cert_uses_plain_sum(int DT, int W)
-{
-    return W >= kCertMinW && DT >= 0;
-}
+// Where the certified sum replaces the cascade (both dtypes), measured
+// against it kernel by kernel: the backward from W = 5 (at W = 4 the
+// cascade, in its two-CTA kernel, was faster: 0.83 of peak against 0.70),
+// the forward from W = 4.
+constexpr int kCertMinWBwd = 5;
+constexpr int kCertMinWFwd = 4;
 template <int DT>
 __host__ __device__ constexpr float cert_factor()
 {

@@ -1,8 +1,8 @@
 // kernels_w.cu - instances of the backward's main kernel for widths W other
 // than 3 (one rows-per-stage choice, R = 6; R = 8 at W = 8), for the strided
 // entry points, which accept 1 <= W <= 8. Widths from 4 up keep 4 channels
-// per thread so their W accumulators per channel stay in registers; widths 4
-// and 5 run two CTAs per SM under the matching register bound; widths from 6
+// per thread so their W accumulators per channel stay in registers; width 4
+// runs two CTAs per SM under the matching register bound; widths from 6
 // split the register file by warpgroup when an H-block needs more than one
 // consumer warpgroup (mcc1d_bwd_main_rs), else run the plain one-CTA form.
 // Compiled apart from kernels.cu so the two build in parallel.

@@ -20,7 +20,7 @@ namespace mcc1d {
 
 constexpr int kW = 3;                 // the only kernel width the operator page supports
 constexpr int kMaxW = 8;              // widest kernel the strided entry points accept
-constexpr int kTwoCtaMaxW = 5;        // widths 4 .. kTwoCtaMaxW run two CTAs per SM
+constexpr int kTwoCtaMaxW = 4;        // widths 4 .. kTwoCtaMaxW run two CTAs per SM
 constexpr int kRegsOneCta = 168;      // register bound of the main kernel (288 threads, one CTA)
 constexpr int kRegsTwoCta = 96;       // ... and of its two-CTA form (mcc1d_bwd_main_x2)
 // From W = kSplitMinW the backward's main kernel splits the register file by
