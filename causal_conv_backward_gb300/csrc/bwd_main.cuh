@@ -181,7 +181,7 @@ __device__ bool consume(const MainParams &p, uint8_t *smem, int64_t r0, int64_t 
     // Wide kernels (kCertMinWBwd): gradX by a certified plain sum, the
     // cascade only where the certificate fails (see below).
     constexpr bool kCF = W >= kCertMinWBwd && !BS;
-    constexpr float kCert = cert_factor<DT>();
+    constexpr float kCert = cert_factor<DT, W>();
     // the fallback finds the W-1 rows before a stage in the previous slot,
     // whose look-ahead holds R rows; one failure bit per (row, channel pair)
     static_assert(!kCF || W - 1 <= R, "certified sums need W - 1 <= R");

@@ -330,28 +330,40 @@ __device__ __forceinline__ float2 mul_ru(float2 a, float2 b)
     return make_float2(__fmul_ru(a.x, b.x), __fmul_ru(a.y, b.y));
 }
 
-// Certificate for a sum s of W <= 8 exact products p_k = g_k w_k in a tree
-// of depth 3 (dot_tree): with a = sum_k |p_k|, |s - exact| <= gamma_3 * a <=
-// 3u(1 + 4u) a (Higham, "Accuracy and Stability of Numerical Algorithms",
-// 2nd ed., section 4.2; u = 2^-24). The 16-bit grid's spacing at x exceeds
-// x * 2^-(m+1) (m + 1 significant bits: 11 for fp16, 8 for bf16), so if
-// that error bound is below (|s| - bound) * 2^-(m+1), s and the exact sum lie
-// closer than the smallest spacing between them: at most one rounding
-// boundary separates them and round(s) is within 1 ulp of the exact sum
-// rounded once. The kernels test kCert * max_k|w_k| * sum_k|g_k| <= |s|,
-// whose left side, formed with upward rounding, is at least kCert * a, so
-// the factor's last (1 + 2^-20) is margin.
 // Where the certified sum replaces the cascade (both dtypes), measured
 // against it kernel by kernel: the backward from W = 5 (at W = 4 the
 // cascade, in its two-CTA kernel, was faster: 0.83 of peak against 0.70),
 // the forward from W = 4.
 constexpr int kCertMinWBwd = 5;
 constexpr int kCertMinWFwd = 4;
-template <int DT>
+
+// Certificate for a sum s of W <= 8 exact products p_k = g_k w_k formed by
+// dot_tree, a = sum_k |p_k|, u = 2^-24. Each addition's rounding error is
+// at most u times its computed result (Higham, "Accuracy and Stability of
+// Numerical Algorithms", 2nd ed., (2.5)), and s - exact is the sum of those
+// errors. The nodes of one level of the tree below the root cover disjoint
+// sets of products, so their magnitudes add up to at most a (1 + 2u): with
+// L such levels (L = 1 up to W = 4: the pairs; L = 2 for W = 5..8: the
+// pairs, then the pairs' pairs or an odd product fused into the last pair),
+//     |s - exact| <= u (L a (1 + 2u) + |s|) =: E.
+// The 16-bit grid's spacing at x exceeds x * 2^-(m+1) (m + 1 significant
+// bits: 11 for fp16, 8 for bf16), so if E < (|s| - E) 2^-(m+1), s and the
+// exact sum lie closer than the smallest spacing between them: at most one
+// rounding boundary separates them and round(s) is within 1 ulp of the exact
+// sum rounded once. Solved for |s| that is
+//     |s| > L a u 2^(m+1) (1 + 2^-(m+1)) / (1 - u 2^(m+1) (1 + 2^-(m+1))) (1 + 2u),
+// which cert_factor<DT, W>() * a covers (the last factor and the rounding of
+// the constants within its (1 + 2^-20)). The kernels test
+// cert_factor * max_k|w_k| * sum_k|g_k| <= |s|, whose left side, formed
+// with upward rounding, is at least cert_factor * a.
+template <int DT, int W>
 __host__ __device__ constexpr float cert_factor()
 {
-    // 3 * 2^-24 * 2^(m+1) / (1 - 2^-m) * (1 + 2^-20), rounded up
-    return DT == 1 ? 3.f * 1.220703125e-4f * 1.0011f : 3.f * 1.52587890625e-5f * 1.0081f;
+    static_assert(W >= 1 && W <= 8, "dot_tree's levels are counted for W <= 8");
+    constexpr float kL = W <= 4 ? 1.f : 2.f;
+    // u 2^(m+1) = 2^-13 (fp16), 2^-16 (bf16); the quotient times (1 + 2^-20)
+    // is 1.000611 (fp16) and 1.003923 (bf16), rounded up here
+    return DT == 1 ? kL * 1.220703125e-4f * 1.00062f : kL * 1.52587890625e-5f * 1.00393f;
 }
 
 // ------------------------------------------------------------------ row cursor

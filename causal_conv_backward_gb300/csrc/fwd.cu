@@ -183,7 +183,7 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
     // only for channels whose certificate fails, recomputed after the stage
     // from the staged rows (the slot keeps x rows: not with bulk stores).
     constexpr bool kCF = W >= kCertMinWFwd && !BS;
-    constexpr float kCert = cert_factor<DT>();
+    constexpr float kCert = cert_factor<DT, W>();
     // the W-1 rows before a stage that follows a full stage are the previous
     // slot's last rows; one failure bit per (row, channel pair)
     static_assert(!kCF || W - 1 <= R, "certified sums need W - 1 <= R");

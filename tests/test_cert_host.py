@@ -1,8 +1,8 @@
-"""The certificate of the wide kernels' plain sum (widths 6..8).
+"""The certificate of the wide kernels' plain sum (widths 4..8).
 
-At W >= 6 the backward's and the forward's main kernels sum the W exact fp32
-products of a value in a fixed tree of depth 3 (pairs by a multiply and a
-fused multiply-add, then the pairs' tree) and keep the result when
+From W = 5 (backward) and W = 4 (forward) the main kernels sum the W exact
+fp32 products of a value in a fixed tree (pairs by a multiply and a fused
+multiply-add, then the pairs' tree) and keep the result when
 cert_factor * max_k|w_k| * sum_k|g_k| (formed with upward rounding) <= |sum|;
 otherwise the channel is recomputed with the compensated cascade. The claim
 is that every kept value, rounded once to the 16-bit type, is within 1 ulp of
@@ -29,41 +29,52 @@ HEADER = os.path.join(ROOT, "causal_conv_backward_gb300", "csrc", "device_common
 MBITS = {"fp16": 10, "bf16": 7}
 
 
-def header_factors():
-    """(fp16 factor, bf16 factor) as written in cert_factor<DT>()."""
+def header_factor(dt: str, W: int) -> float:
+    """cert_factor<DT, W>() as written in the header: the return expression
+    with its level count kL (itself a function of W) substituted."""
     txt = open(HEADER).read()
     body = txt[txt.index("constexpr float cert_factor()"):]
-    body = body[:body.index("}")]
+    body = body[:body.index("\n}")]
+    m = re.search(r"kL = W <= (\d+) \? ([\d.]+)f : ([\d.]+)f;", body)
+    assert m, "cert_factor's level count not found"
+    L = float(m.group(2)) if W <= int(m.group(1)) else float(m.group(3))
     m = re.search(r"DT == 1 \? ([^:]+) : ([^;]+);", body)
     assert m, "cert_factor's expression not found"
 
     def ev(expr):
-        terms = [t.strip().rstrip("f") for t in expr.split("*")]
         v = 1.0
-        for t in terms:
-            v *= float(t)
+        for t in expr.split("*"):
+            t = t.strip().rstrip("f")
+            v *= L if t == "kL" else float(t)
         return v
 
-    return ev(m.group(1)), ev(m.group(2))
+    return ev(m.group(1) if dt == "fp16" else m.group(2))
 
 
-def needed_factor(mbits):
-    """Smallest factor the argument accepts: gamma_3 (three roundings of
-    u = 2^-24 on any path of a depth-3 tree) against half the 16-bit
-    relative spacing 2^-(m+1), with the distance |s| - bound; the last
-    (1 + 2^-20) is margin (the kernels form their bound with upward rounding)."""
+def levels(W: int) -> int:
+    """Levels of the kernels' tree below the root whose nodes round (see
+    tree()): W <= 4 the pairs only; W = 5..8 the pairs and one more."""
+    return 1 if W <= 4 else 2
+
+
+def needed_factor(mbits: int, W: int) -> float:
+    """Smallest factor the argument accepts: |s - exact| <= u (L a (1 + 2u)
+    + |s|) must stay below (|s| - that) * 2^-(m+1), half the 16-bit relative
+    spacing; the last (1 + 2^-20) is margin."""
     u = 2.0 ** -24
-    gamma3 = 3 * u / (1 - 3 * u)
-    return gamma3 * 2.0 ** (mbits + 1) / (1 - 2.0 ** -mbits) * (1 + 2.0 ** -20)
+    h = 2.0 ** -(mbits + 1)
+    q = u / h * (1 + h) / (1 - u / h * (1 + h))
+    return levels(W) * q * (1 + 2 * u) * (1 + 2.0 ** -20)
 
 
-def test_header_factors_cover_the_bound():
-    f16, b16 = header_factors()
-    assert np.float32(f16) >= needed_factor(MBITS["fp16"])
-    assert np.float32(b16) >= needed_factor(MBITS["bf16"])
-    # and not loose by more than 0.2 %, which would only cost fallbacks
-    assert f16 <= 1.002 * needed_factor(MBITS["fp16"])
-    assert b16 <= 1.002 * needed_factor(MBITS["bf16"])
+@pytest.mark.parametrize("W", [4, 5, 6, 7, 8])
+def test_header_factors_cover_the_bound(W):
+    for dt in ("fp16", "bf16"):
+        f = header_factor(dt, W)
+        need = needed_factor(MBITS[dt], W)
+        assert np.float32(f) >= need, (dt, W)
+        # and not loose by more than 0.1 %, which would only cost recomputes
+        assert f <= 1.001 * need, (dt, W)
 
 
 def to_bf16(a):
@@ -89,8 +100,8 @@ def ulp16(x, dt):
 def tree(v):
     """The kernels' dot_tree over exact products v[..., 0:W] in float32:
     pairs (2j, 2j+1) rounded once, an odd last product fused into the last
-    pair, then the pairs' tree (W = 6: (P0 + P1) + P2; 7: (P0 + P1) + (P2 + p6);
-    8: (P0 + P1) + (P2 + P3))."""
+    pair, then the pairs' tree (W = 4: P0 + P1; 5: P0 + (P1 + p4); 6:
+    (P0 + P1) + P2; 7: (P0 + P1) + (P2 + p6); 8: (P0 + P1) + (P2 + P3))."""
     f = np.float32
     W = v.shape[1]
     pr = [(v[:, 2 * j] + v[:, 2 * j + 1]).astype(f) for j in range(W // 2)]
@@ -129,10 +140,9 @@ def operands(rng, n, W, dt, cancel):
 
 
 @pytest.mark.parametrize("dt", ["fp16", "bf16"])
-@pytest.mark.parametrize("W", [6, 7, 8])
+@pytest.mark.parametrize("W", [4, 5, 6, 7, 8])
 def test_every_certified_sum_is_within_one_ulp(dt, W):
-    f16, b16 = header_factors()
-    cert = np.float32(f16 if dt == "fp16" else b16)
+    cert = np.float32(header_factor(dt, W))
     rng = np.random.default_rng(1000 * W + (dt == "fp16"))
     kept = failed = 0
     for cancel in (False, True):
@@ -159,3 +169,30 @@ def test_every_certified_sum_is_within_one_ulp(dt, W):
         failed += int((~ok & nz).sum())
     # the simulation exercises both outcomes
     assert kept > 60000 and failed > 1000, (kept, failed)
+
+
+@pytest.mark.parametrize("W", [4, 5, 6, 7, 8])
+def test_tree_error_within_the_level_bound(W):
+    """The error bound the factor rests on, |s - exact| <= u (L a (1 + 2u)
+    + |s|), holds for the tree on random exact products (11-bit by 11-bit
+    significands, mixed signs, exponents over 6 binades: float64 sums are
+    exact); and with one level fewer it would not (W >= 5), so the level
+    count is the one the tree needs."""
+    u = 2.0 ** -24
+    rng = np.random.default_rng(70 + W)
+    worst = worst_fewer = 0.0
+    for _ in range(6):
+        n = 200000
+        sig = rng.integers(1024, 2048, (n, W)).astype(np.float64) * rng.integers(1024, 2048, (n, W))
+        p = (sig * 2.0 ** rng.integers(-24, -18, (n, W)) * rng.choice([-1, 1], (n, W))).astype(np.float32)
+        assert np.array_equal(p.astype(np.float64), sig * 2.0 ** np.round(np.log2(np.abs(p) / sig))
+                              * np.sign(p))                    # products exact in float32
+        s = tree(p).astype(np.float64)
+        p64 = p.astype(np.float64)
+        err, a = np.abs(s - p64.sum(1)), np.abs(p64).sum(1)
+        L = levels(W)
+        worst = max(worst, float(np.max(err / (u * (L * a * (1 + 2 * u) + np.abs(s))))))
+        if L > 1:
+            worst_fewer = max(worst_fewer, float(np.max(err / (u * ((L - 1) * a * (1 + 2 * u) + np.abs(s))))))
+    assert worst <= 1.0, worst
+    assert L == 1 or worst_fewer > 1.0, worst_fewer
