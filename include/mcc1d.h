@@ -339,7 +339,8 @@ int32_t mcc1d_fwd_ex(const mcc1d_fwd_tensors *t, int64_t S, int64_t B, int64_t H
 /*
  * Diagnostics (no counterpart on the page): the execution plan the library
  * would use for a shape, as text lines "key=value" (H-block split, channels
- * per thread, warps, rows per stage, ring depth, CTAs, shared memory,
+ * per thread, warps, whether the main kernel splits its registers by
+ * warpgroup, rows per stage, ring depth, CTAs, shared memory,
  * workspace layout, reduce shape; per-H-block CTA and slot ranges as comma
  * lists). kind: MCC1D_PLAN_BWD (mcc1d_bwd, W = 3), MCC1D_PLAN_BWD_EX (the
  * strided calls, 1 <= W <= 8) or MCC1D_PLAN_FWD (mcc1d_fwd, 1 <= W <= 8; with a GPU the
