@@ -1,6 +1,6 @@
 // kernels_w.cu - instances of the backward's main kernel for widths W other
-// than 3 (one rows-per-stage choice, R = 6; R = 8 at W = 8), for the strided
-// entry points, which accept 1 <= W <= 8. Widths from 4 up keep 4 channels
+// than 3 (one rows-per-stage choice: R = 6; 10 at W = 6, 8 at W = 7, 8), for
+// the strided entry points, which accept 1 <= W <= 8. Widths from 4 up keep 4 channels
 // per thread so their W accumulators per channel stay in registers; width 4
 // runs two CTAs per SM under the matching register bound; widths from 6
 // split the register file by warpgroup when an H-block needs more than one
@@ -13,7 +13,7 @@ namespace mcc1d {
 template <int DT, int W>
 static MainFn pick(int vec, int R, bool split)
 {
-    constexpr int kR = W == kMaxW ? 8 : 6;
+    constexpr int kR = W == 6 ? 10 : W >= 7 ? 8 : 6;
     if (R != kR)
         return nullptr;
     if constexpr (W >= kSplitMinW) {
