@@ -36,7 +36,14 @@
 
 namespace mcc1d {
 
-constexpr int kFwdR = 8;             // output rows per stage
+// Output rows per stage: 8 up to W = 3; wider kernels, bound by their
+// per-stage work rather than HBM, take deeper stages (measured against 8,
+// 10, 12 and 16 in one call: W = 4, 5 best at 12, W >= 6 at 16, the most a
+// stage's 32-bit failure mask holds at 2 channel pairs per thread).
+constexpr int fwd_rows(int W)
+{
+    return W <= 3 ? 8 : W <= 5 ? 12 : 16;
+}
 constexpr int kFwdMaxThreads = 288;  // 8 consumer warps + producer
 constexpr int kFwdMaxStages = 8;
 // 4 KB rows: two ring slots per CTA (more measured slower on this 1:1
@@ -461,12 +468,12 @@ static FwdFn fwd_pick(int vec, bool bulk)
 {
     if constexpr (W == 3) {
         if (vec == 4)
-            return bulk ? nullptr : mcc1d_fwd_main<DT, kFwdR, 2, 3, false>;
-        return bulk ? mcc1d_fwd_main<DT, kFwdR, 4, 3, true> : mcc1d_fwd_main<DT, kFwdR, 4, 3, false>;
+            return bulk ? nullptr : mcc1d_fwd_main<DT, fwd_rows(3), 2, 3, false>;
+        return bulk ? mcc1d_fwd_main<DT, fwd_rows(3), 4, 3, true> : mcc1d_fwd_main<DT, fwd_rows(3), 4, 3, false>;
     } else if constexpr (W >= 6) {
-        return vec == 4 && !bulk ? mcc1d_fwd_main_1<DT, kFwdR, 2, W> : nullptr;
+        return vec == 4 && !bulk ? mcc1d_fwd_main_1<DT, fwd_rows(W), 2, W> : nullptr;
     } else {
-        return vec == 4 && !bulk ? mcc1d_fwd_main<DT, kFwdR, 2, W, false> : nullptr;
+        return vec == 4 && !bulk ? mcc1d_fwd_main<DT, fwd_rows(W), 2, W, false> : nullptr;
     }
 }
 
@@ -499,11 +506,11 @@ bool fwd_bulk_store(const Plan &pl)
 
 FwdRing fwd_ring(const Plan &pl)
 {
-    // kFwdR output rows per slot, one W-1-row halo area; as many slots as
-    // the CTA's share of shared memory allows, 2 .. kFwdMaxStages
+    // fwd_rows(W) output rows per slot, one W-1-row halo area; as many slots
+    // as the CTA's share of shared memory allows, 2 .. kFwdMaxStages
     FwdRing r;
-    r.rows_per_stage = kFwdR;
-    r.slot_bytes = (uint32_t)kFwdR * pl.row_bytes;
+    r.rows_per_stage = fwd_rows(pl.W);
+    r.slot_bytes = (uint32_t)r.rows_per_stage * pl.row_bytes;
     const uint32_t halo_bytes = (uint32_t)(pl.W - 1) * pl.row_bytes;
     int64_t budget = kSmemPerSM / pl.ctas_per_sm - kSmemReservedPerCta;
     if (budget > kSmemDynMax)
