@@ -1,5 +1,5 @@
 // kernels_w.cu - instances of the backward's main kernel for widths W other
-// than 3 (one rows-per-stage choice: R = 6; 10 at W = 6, 8 at W = 7, 8), for
+// than 3 (one rows-per-stage choice: R = 6; 10 at W = 4, 6, 8 at W = 7, 8), for
 // the strided entry points, which accept 1 <= W <= 8. Widths from 4 up keep 4 channels
 // per thread so their W accumulators per channel stay in registers; width 4
 // runs two CTAs per SM under the matching register bound; widths from 6
@@ -13,7 +13,7 @@ namespace mcc1d {
 template <int DT, int W>
 static MainFn pick(int vec, int R, bool split)
 {
-    constexpr int kR = W == 6 ? 10 : W >= 7 ? 8 : 6;
+    constexpr int kR = W == 4 || W == 6 ? 10 : W >= 7 ? 8 : 6;
     if (R != kR)
         return nullptr;
     if constexpr (W >= kSplitMinW) {
@@ -24,7 +24,7 @@ static MainFn pick(int vec, int R, bool split)
         if (split)
             return nullptr;
         if constexpr (W >= 4 && W <= kTwoCtaMaxW)
-            return vec == 4 ? mcc1d_bwd_main_x2<DT, 6, 2, W> : nullptr;
+            return vec == 4 ? mcc1d_bwd_main_x2<DT, kR, 2, W> : nullptr;
         else if constexpr (W >= 4)
             return vec == 4 ? mcc1d_bwd_main<DT, 6, 2, W> : nullptr;
         else
