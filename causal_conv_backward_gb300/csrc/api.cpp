@@ -244,10 +244,11 @@ int32_t fwd_plan(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, Plan
     st = make_plan_for(S, B, H, W, dtype, o, p);
     if (st != kOk)
         return st;
-    o.regs_bound = fwd_kernel_regs(p->dtype, p->vec, p->W, fwd_bulk_store(*p));
-    if (o.regs_bound > 0)
-        st = make_plan_for(S, B, H, W, dtype, o, p);
-    return st;
+    // then CTAs per SM within the kernel's registers (as the runtime reports
+    // them) and within shared memory for its smallest ring (two slots)
+    o.regs_bound = fwd_kernel_regs(p->dtype, p->vec, p->W, fwd_variant(*p));
+    o.smem_min_per_cta = (int)fwd_ring_min_bytes(*p);
+    return make_plan_for(S, B, H, W, dtype, o, p);
 }
 
 }  // namespace

@@ -28,6 +28,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "device.h"
@@ -37,13 +38,15 @@
 namespace mcc1d {
 
 // Output rows per stage: 8 up to W = 3; wider kernels, bound by their
-// per-stage work rather than HBM, take deeper stages (measured against 8,
-// 10, 12 and 16 in one call: W = 4, 5 best at 12, W >= 6 at 16, the most a
-// stage's 32-bit failure mask holds at 2 channel pairs per thread).
-constexpr int fwd_rows(int W)
+// per-stage work rather than HBM, take deeper stages (measured in one call
+// against 8, 10, 12 and 16, and 20 and 24 from W = 6: W = 4, 5 best at 12;
+// W >= 6 at 24 on H-blocks over 512 channels (`deep`), at 16 on narrower
+// ones, where fewer consumer warps share the ring).
+constexpr int fwd_rows(int W, bool deep)
 {
-    return W <= 3 ? 8 : W <= 5 ? 12 : 16;
+    return W <= 3 ? 8 : W <= 5 ? 12 : deep ? 24 : 16;
 }
+constexpr int kFwdDeepMinHbWidth = 576;   // channels of an H-block that take deep stages
 constexpr int kFwdMaxThreads = 288;  // 8 consumer warps + producer
 constexpr int kFwdMaxStages = 8;
 // 4 KB rows: two ring slots per CTA (more measured slower on this 1:1
@@ -194,7 +197,9 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
     // the W-1 rows before a stage that follows a full stage are the previous
     // slot's last rows; one failure bit per (row, channel pair)
     static_assert(!kCF || W - 1 <= R, "certified sums need W - 1 <= R");
-    static_assert(!kCF || R * NP <= 32, "one 32-bit failure mask per stage");
+    static_assert(!kCF || R * NP <= 64, "one 64-bit failure mask per stage");
+    // the stage's failure mask: one bit per (row, channel pair)
+    using FailMask = typename std::conditional<(R * NP > 32), unsigned long long, uint32_t>::type;
     const int NS = p.stages;
     const uint32_t bar_full0 = smem_u32(smem + p.off_bar);
     const uint32_t bar_empty0 = bar_full0 + 8u * (uint32_t)NS;
@@ -273,7 +278,7 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                 }
             }
             uint8_t *yp = p.y + 2 * (((cur.i * p.B + cur.j) * p.H) + (int64_t)hb_cur * p.hb_width + CH * ct);
-            uint32_t fails = 0;
+            FailMask fails = 0;
             auto row = [&](int r) {
                 const Vf<NP> xn = unpack<DT, NP>(load_raw<NP>(xs + (size_t)r * p.row_bytes));
                 const uint32_t keep = 0u - (uint32_t)ms[r + WH];
@@ -290,7 +295,7 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                         const float2 lim = mul_ru(kmw[e], gr);
                         const bool ok = (lim.x <= fabsf(sf.x)) & (lim.y <= fabsf(sf.y));
                         o[e] = pack2<DT>(sf) & keep;
-                        fails |= (ok ? 0u : 1u) << (r * NP + e);
+                        fails |= (FailMask)(ok ? 0u : 1u) << (r * NP + e);
                         gab[e] = sub_abs_ru(gr, win[0].e[e]);   // x(t+r-W+1) leaves the window
                     } else {
                         // exact fp32 products, summed and rounded once by
@@ -335,7 +340,11 @@ __device__ bool fwd_consume(const FwdParams &p, uint8_t *smem, int64_t r0, int64
                 const uint8_t *hs = smem + p.off_halo + 2 * CH * ct;
                 const uint8_t *psl = smem + (size_t)(prev_slot < 0 ? 0 : prev_slot) * p.slot_bytes + 2 * CH * ct;
                 while (fails) {
-                    const int b = __ffs(fails) - 1;
+                    int b;
+                    if constexpr (R * NP > 32)
+                        b = __ffsll((long long)fails) - 1;
+                    else
+                        b = __ffs((int)fails) - 1;
                     fails &= fails - 1;
                     const int r = b / NP, e = b % NP;
                     float2 qk[W];
@@ -464,38 +473,43 @@ typedef void (*FwdFn)(FwdParams);
 // thread (their plan keeps H-blocks of at most 1024 channels), from W = 6 in
 // the one-CTA form.
 template <int DT, int W>
-static FwdFn fwd_pick(int vec, bool bulk)
+static FwdFn fwd_pick(int vec, int variant)
 {
     if constexpr (W == 3) {
         if (vec == 4)
-            return bulk ? nullptr : mcc1d_fwd_main<DT, fwd_rows(3), 2, 3, false>;
-        return bulk ? mcc1d_fwd_main<DT, fwd_rows(3), 4, 3, true> : mcc1d_fwd_main<DT, fwd_rows(3), 4, 3, false>;
+            return variant != kFwdPlain ? nullptr : mcc1d_fwd_main<DT, fwd_rows(3, false), 2, 3, false>;
+        return variant == kFwdBulkStores ? mcc1d_fwd_main<DT, fwd_rows(3, false), 4, 3, true>
+             : variant == kFwdPlain      ? mcc1d_fwd_main<DT, fwd_rows(3, false), 4, 3, false>
+                                         : nullptr;
     } else if constexpr (W >= 6) {
-        return vec == 4 && !bulk ? mcc1d_fwd_main_1<DT, fwd_rows(W), 2, W> : nullptr;
+        if (vec != 4 || variant == kFwdBulkStores)
+            return nullptr;
+        return variant == kFwdDeep ? mcc1d_fwd_main_1<DT, fwd_rows(W, true), 2, W>
+                                   : mcc1d_fwd_main_1<DT, fwd_rows(W, false), 2, W>;
     } else {
-        return vec == 4 && !bulk ? mcc1d_fwd_main<DT, fwd_rows(W), 2, W, false> : nullptr;
+        return vec == 4 && variant == kFwdPlain ? mcc1d_fwd_main<DT, fwd_rows(W, false), 2, W, false> : nullptr;
     }
 }
 
 template <int DT>
-static FwdFn fwd_pick_w(int vec, int W, bool bulk)
+static FwdFn fwd_pick_w(int vec, int W, int variant)
 {
     switch (W) {
-    case 1: return fwd_pick<DT, 1>(vec, bulk);
-    case 2: return fwd_pick<DT, 2>(vec, bulk);
-    case 3: return fwd_pick<DT, 3>(vec, bulk);
-    case 4: return fwd_pick<DT, 4>(vec, bulk);
-    case 5: return fwd_pick<DT, 5>(vec, bulk);
-    case 6: return fwd_pick<DT, 6>(vec, bulk);
-    case 7: return fwd_pick<DT, 7>(vec, bulk);
-    case 8: return fwd_pick<DT, 8>(vec, bulk);
+    case 1: return fwd_pick<DT, 1>(vec, variant);
+    case 2: return fwd_pick<DT, 2>(vec, variant);
+    case 3: return fwd_pick<DT, 3>(vec, variant);
+    case 4: return fwd_pick<DT, 4>(vec, variant);
+    case 5: return fwd_pick<DT, 5>(vec, variant);
+    case 6: return fwd_pick<DT, 6>(vec, variant);
+    case 7: return fwd_pick<DT, 7>(vec, variant);
+    case 8: return fwd_pick<DT, 8>(vec, variant);
     default: return nullptr;
     }
 }
 
-static FwdFn fwd_kernel(int dtype, int vec, int W, bool bulk)
+static FwdFn fwd_kernel(int dtype, int vec, int W, int variant)
 {
-    return dtype == 0 ? fwd_pick_w<0>(vec, W, bulk) : fwd_pick_w<1>(vec, W, bulk);
+    return dtype == 0 ? fwd_pick_w<0>(vec, W, variant) : fwd_pick_w<1>(vec, W, variant);
 }
 
 bool fwd_bulk_store(const Plan &pl)
@@ -504,12 +518,26 @@ bool fwd_bulk_store(const Plan &pl)
            pl.rows_total / pl.ncta >= kFwdBulkStoreMinRowsPerCta;
 }
 
+int fwd_variant(const Plan &pl)
+{
+    if (fwd_bulk_store(pl))
+        return kFwdBulkStores;
+    return pl.W >= 6 && pl.hb_width >= kFwdDeepMinHbWidth ? kFwdDeep : kFwdPlain;
+}
+
+uint32_t fwd_ring_min_bytes(const Plan &pl)
+{
+    // as fwd_ring below with two slots
+    const uint32_t slot = (uint32_t)fwd_rows(pl.W, fwd_variant(pl) == kFwdDeep) * pl.row_bytes;
+    return 2u * (slot + 48u) + 64u + (uint32_t)(pl.W - 1) * pl.row_bytes;
+}
+
 FwdRing fwd_ring(const Plan &pl)
 {
     // fwd_rows(W) output rows per slot, one W-1-row halo area; as many slots
     // as the CTA's share of shared memory allows, 2 .. kFwdMaxStages
     FwdRing r;
-    r.rows_per_stage = fwd_rows(pl.W);
+    r.rows_per_stage = fwd_rows(pl.W, fwd_variant(pl) == kFwdDeep);
     r.slot_bytes = (uint32_t)r.rows_per_stage * pl.row_bytes;
     const uint32_t halo_bytes = (uint32_t)(pl.W - 1) * pl.row_bytes;
     int64_t budget = kSmemPerSM / pl.ctas_per_sm - kSmemReservedPerCta;
@@ -531,20 +559,20 @@ FwdRing fwd_ring(const Plan &pl)
     return r;
 }
 
-int fwd_kernel_regs(int dtype, int vec, int W, bool bulk)
+int fwd_kernel_regs(int dtype, int vec, int W, int variant)
 {
     // registers per thread of the forward instance (cached per device and
     // instance; 0 when the runtime cannot say)
-    static std::atomic<int> cache[64][8 * (kMaxW + 1)];
+    static std::atomic<int> cache[64][12 * (kMaxW + 1)];
     if (W < 1 || W > kMaxW)
         return 0;
-    const FwdFn fn = fwd_kernel(dtype, vec, W, bulk);
+    const FwdFn fn = fwd_kernel(dtype, vec, W, variant);
     if (fn == nullptr)
         return 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 0;
-    const int slot = ((dtype * 2 + (vec == 4 ? 1 : 0)) * 2 + (bulk ? 1 : 0)) * (kMaxW + 1) + W;
+    const int slot = ((dtype * 2 + (vec == 4 ? 1 : 0)) * 3 + variant) * (kMaxW + 1) + W;
     std::atomic<int> &c = cache[dev & 63][slot];
     int r = c.load(std::memory_order_acquire);
     if (r > 0)
@@ -590,14 +618,14 @@ int32_t launch_fwd(const Plan &pl, const Layout &L, const void *x, const void *w
     fp.w_vec = (L.w[1] == 1 && (L.w[0] * 2) % 16 == 0 && ((uintptr_t)weight & 15u) == 0) ? 1 : 0;
     fp.contig_rows = (pl.B == 1 && pl.n_hb == 1 && L.x[0] == pl.H && !long_ranges(pl)) ? 1 : 0;
 
-    const bool bulk = fwd_bulk_store(pl);
-    FwdFn fn = fwd_kernel(pl.dtype, pl.vec, pl.W, bulk);
+    const int variant = fwd_variant(pl);
+    FwdFn fn = fwd_kernel(pl.dtype, pl.vec, pl.W, variant);
     if (fn == nullptr)
         return kErrCuda;
     // the shared-memory attribute, once per (instance, device, context): a
     // context created after a device reset starts without it
-    static std::atomic<unsigned long long> done[8 * (kMaxW + 1)][64];
-    const int slot_id = ((pl.dtype * 2 + (pl.vec == 4 ? 1 : 0)) * 2 + (bulk ? 1 : 0)) * (kMaxW + 1) + pl.W;
+    static std::atomic<unsigned long long> done[12 * (kMaxW + 1)][64];
+    const int slot_id = ((pl.dtype * 2 + (pl.vec == 4 ? 1 : 0)) * 3 + variant) * (kMaxW + 1) + pl.W;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return kErrCuda;

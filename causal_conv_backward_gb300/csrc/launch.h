@@ -40,16 +40,23 @@ struct FwdRing {
     uint32_t slot_bytes, off_halo, off_mask, off_bar, smem_bytes;
 };
 FwdRing fwd_ring(const Plan &p);
+// Shared memory of the forward's smallest ring (two slots) for plan `p`.
+uint32_t fwd_ring_min_bytes(const Plan &p);
 // Whether the forward stores y rows with bulk copies out of its ring (wide
 // rows) rather than with per-thread stores.
 bool fwd_bulk_store(const Plan &p);
+// The forward kernel's form for plan `p`: plain, bulk y stores (wide rows at
+// W = 3), or deep stages (W >= 6 on H-blocks of kFwdDeepMinHbWidth channels
+// and more).
+enum { kFwdPlain = 0, kFwdBulkStores = 1, kFwdDeep = 2 };
+int fwd_variant(const Plan &p);
 // One thread waiting on an mbarrier with the library's bounded wait; writes
 // kOk (arrive != 0: it arrives first) or kErrTimeout (nothing arrives) to the
 // device word `status`.
 int32_t launch_wait_selftest(int32_t *status, int32_t arrive, cudaStream_t stream);
 // Registers per thread of the forward kernel instance for (dtype, vec, W,
-// bulk stores), from the runtime (0 when unknown).
-int fwd_kernel_regs(int dtype, int vec, int W, bool bulk);
+// fwd_variant), from the runtime (0 when unknown).
+int fwd_kernel_regs(int dtype, int vec, int W, int variant);
 // Enqueues the forward kernel of plan `p`; the inputs are read with layout L
 // (x with unit H stride and 16-byte aligned rows), y is dense. `status` is a
 // device word the kernel ORs kErrTimeout into if a wait gives up, or null.

@@ -120,6 +120,10 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
         while (cps > 1 && cps * (p->threads / 32) > warps_per_sm)
             --cps;
     }
+    // ... and no more than the shared memory holds at the kernel's minimum
+    if (o.smem_min_per_cta > 0)
+        while (cps > 1 && (int64_t)cps * (o.smem_min_per_cta + kSmemReservedPerCta) > kSmemPerSM)
+            --cps;
     p->ctas_per_sm = cps;
 
     p->row_bytes = (uint32_t)p->hb_width * 2u;

@@ -158,6 +158,7 @@ struct PlanOpts {
     int vec4_max_warps;          // 4 channels per thread allowed up to this many consumer warps
     bool vec4_always;            // ... and taken whenever allowed (else only for better lane use)
     bool reg_split = false;      // producer warpgroup + whole consumer warpgroups (setmaxnreg)
+    int smem_min_per_cta = 0;    // shared memory a CTA cannot run without; CTAs per SM capped to fit (0: none)
 };
 int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype, const PlanOpts &o,
                       Plan *p);
