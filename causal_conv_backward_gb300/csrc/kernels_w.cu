@@ -2,9 +2,10 @@
 // than 3 (one rows-per-stage choice: R = 6; 10 at W = 4, 6, 8 at W = 7, 8), for
 // the strided entry points, which accept 1 <= W <= 8. Widths from 4 up keep 4 channels
 // per thread so their W accumulators per channel stay in registers; width 4
-// runs two CTAs per SM under the matching register bound; widths from 6
-// split the register file by warpgroup when an H-block needs more than one
-// consumer warpgroup (mcc1d_bwd_main_rs), else run the plain one-CTA form.
+// runs two CTAs per SM under the matching register bound; width 5 runs the
+// plain one-CTA form, and widths from 6 split the register file by
+// warpgroup when an H-block needs more than one consumer warpgroup
+// (mcc1d_bwd_main_rs), else run the plain one-CTA form too.
 // Compiled apart from kernels.cu so the two build in parallel.
 #include "bwd_main.cuh"
 
