@@ -1,11 +1,10 @@
 // kernels_w.cu - instances of the backward's main kernel for widths W other
-// than 3 (one rows-per-stage choice: R = 6; 10 at W = 4, 6, 8 at W = 7, 8), for
+// than 3 (one rows-per-stage choice: R = 6; 10 at W = 4..6, 8 at W = 7, 8), for
 // the strided entry points, which accept 1 <= W <= 8. Widths from 4 up keep 4 channels
 // per thread so their W accumulators per channel stay in registers; width 4
-// runs two CTAs per SM under the matching register bound; width 5 runs the
-// plain one-CTA form, and widths from 6 split the register file by
-// warpgroup when an H-block needs more than one consumer warpgroup
-// (mcc1d_bwd_main_rs), else run the plain one-CTA form too.
+// runs two CTAs per SM under the matching register bound; widths from 5
+// split the register file by warpgroup when an H-block needs more than one
+// consumer warpgroup (mcc1d_bwd_main_rs), else run the plain one-CTA form.
 // Compiled apart from kernels.cu so the two build in parallel.
 #include "bwd_main.cuh"
 
@@ -14,7 +13,7 @@ namespace mcc1d {
 template <int DT, int W>
 static MainFn pick(int vec, int R, bool split)
 {
-    constexpr int kR = W == 4 || W == 6 ? 10 : W >= 7 ? 8 : 6;
+    constexpr int kR = W >= 4 && W <= 6 ? 10 : W >= 7 ? 8 : 6;   // as the plan's rows per stage
     if (R != kR)
         return nullptr;
     if constexpr (W >= kSplitMinW) {
@@ -27,9 +26,9 @@ static MainFn pick(int vec, int R, bool split)
         if constexpr (W >= 4 && W <= kTwoCtaMaxW)
             return vec == 4 ? mcc1d_bwd_main_x2<DT, kR, 2, W> : nullptr;
         else if constexpr (W >= 4)
-            return vec == 4 ? mcc1d_bwd_main<DT, 6, 2, W> : nullptr;
+            return vec == 4 ? mcc1d_bwd_main<DT, kR, 2, W> : nullptr;
         else
-            return vec == 4 ? mcc1d_bwd_main<DT, 6, 2, W> : mcc1d_bwd_main<DT, 6, 4, W>;
+            return vec == 4 ? mcc1d_bwd_main<DT, kR, 2, W> : mcc1d_bwd_main<DT, kR, 4, W>;
     }
 }
 

@@ -134,7 +134,7 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
 
     // Rows per stage and ring depth: the deepest R (fewer barrier round trips)
     // that still leaves a ring of three slots, else the last choice with what
-    // fits. Widths other than 3 have one instance: R = 6, or 10 at W = 4, 6
+    // fits. Widths other than 3 have one instance: R = 6, or 10 at W = 4..6
     // and 8 at W = 7, 8. Long CTA ranges copy one row per bulk copy (see
     // long_ranges()); narrow rows (4 channels per thread) then spend most of
     // the producer's time per stage, not per byte, so they take R = 14
@@ -144,11 +144,11 @@ int32_t make_plan_for(int64_t S, int64_t B, int64_t H, int64_t W, int32_t dtype,
     if (ncta_est > ceil_div(rows_all, kMinRowsPerCta))
         ncta_est = ceil_div(rows_all, kMinRowsPerCta);
     const bool deep = W == 3 && p->vec == 4 && rows_all / ncta_est >= kDeepMinRowsPerCta;
-    // (deeper stages measured faster for W = 4 (10 rows), 6 (10) and 7, 8
-    // (8); from W = 6 the certified gradX sum also rereads the W-1 window
-    // rows from the previous stage's slot, which holds R look-ahead rows)
-    const int r_w3[3] = {8, 6, 4}, r_deep[4] = {14, 8, 6, 4}, r_other[1] = {6}, r_w46[1] = {10}, r_w78[1] = {8};
-    const int *r_choices = deep ? r_deep : W == 3 ? r_w3 : (W == 4 || W == 6) ? r_w46 : W >= 7 ? r_w78 : r_other;
+    // (deeper stages measured faster for W = 4..6 (10 rows) and 7, 8 (8);
+    // from W = 5 the certified gradX sum also rereads the W-1 window rows
+    // from the previous stage's slot, which holds R look-ahead rows)
+    const int r_w3[3] = {8, 6, 4}, r_deep[4] = {14, 8, 6, 4}, r_other[1] = {6}, r_w10[1] = {10}, r_w78[1] = {8};
+    const int *r_choices = deep ? r_deep : W == 3 ? r_w3 : (W >= 4 && W <= 6) ? r_w10 : W >= 7 ? r_w78 : r_other;
     const int n_choices = deep ? 4 : W == 3 ? 3 : 1;
     p->rows_per_stage = 0;
     for (int t = 0; t < n_choices; ++t) {

@@ -30,7 +30,7 @@ constexpr int kRegsTwoCta = 96;       // ... and of its two-CTA form (mcc1d_bwd_
 // kSplitConsumerRegs. The consumers' share must come from what the producer
 // group gives up: 128 * 56 + 256 * 224 = 384 * 168 exactly at the widest
 // plan (8 consumer warps), less for narrower ones.
-constexpr int kSplitMinW = 6;
+constexpr int kSplitMinW = 5;
 constexpr int kSplitProducerThreads = 128;
 constexpr int kSplitLaunchRegs = 168;
 constexpr int kSplitProducerRegs = 56;

@@ -78,9 +78,9 @@ def check_bwd(p, S, B, H, W):
     check_common(p, S, B, H, W)
     assert W < 4 or (p["vec"] == 4 and p["hb_width"] <= 1024)
     R = p["rows_per_stage"]
-    assert R in ((4, 6, 8, 14) if W == 3 else (10,) if W in (4, 6) else (8,) if W >= 7 else (6,))
-    assert W < 6 or W - 1 <= R        # the certified sum's fallback reads the previous slot
-    assert p["reg_split"] == (1 if W >= 6 and cdiv(p["hb_width"] // p["vec"], 32) > 4 else 0)
+    assert R in ((4, 6, 8, 14) if W == 3 else (10,) if W in (4, 5, 6) else (8,) if W >= 7 else (6,))
+    assert W < 5 or W - 1 <= R        # the certified sum's fallback reads the previous slot
+    assert p["reg_split"] == (1 if W >= 5 and cdiv(p["hb_width"] // p["vec"], 32) > 4 else 0)
     assert R != 14 or p["vec"] == 4
     assert 2 * R + W - 1 <= 32               # one producer lane per staged row
     assert p["slot_bytes"] == (2 * R + W - 1) * p["row_bytes"]
